@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of the Kimi K3 latent routed-MoE layer forward on GB300.
+
+One step = one forward of the whole layer (router, top-k, permutation, expert
+GEMMs, combine + RMSNorm, up-projection, shared experts when configured) over
+one batch of synthetic tokens, inputs resident in HBM, L2 flushed (512 MB
+write) between steps outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+Default workload: the K3 decode batch of 16 tokens (configs[1]).  Under
+torchrun every rank runs an independent replica on its own GPU (the layer is
+token-parallel; no collective on the data path); the time is the max over
+ranks and the value counts the tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode expert-weight GB/s vs HBM peak; prefill TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+EXPERT_BYTES = None   # set per config
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_name(cfg):
+    s = (f"{cfg.name}: T={cfg.T} tokens, hidden {cfg.H}, latent {cfg.L}, {cfg.E} experts top-{cfg.K}, "
+         f"expert inter {cfg.I}, MXFP4 experts, router {cfg.router_dtype}")
+    if cfg.S:
+        s += f", shared GLU {cfg.H}->{cfg.S}->{cfg.H} MXFP4"
+    if cfg.select_bias:
+        s += ", Zipf(1.1) selection bias"
+    return s
+
+
+# ------------------------------------------------------------------ accounting
+def stage_work(cfg, touched, path_tensor):
+    """Algorithmic bytes and flops per forward, per stage."""
+    T, H, L, E, K, I, S = cfg.T, cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S
+    R = T * K
+    rb = 2 if cfg.router_dtype == "bf16" else 4
+    act_b = 2 if path_tensor else 4
+    mx = lambda rows, cols: rows * cols // 2 + rows * cols // 32
+    w = {}
+    w["router"] = (E * H * rb + T * H * 2 + T * E * 4, 2 * T * E * H)
+    w["down_proj"] = (L * H * 2 + T * H * 2 + T * L * 2, 2 * T * L * H)
+    w["topk"] = (T * E * 4 + R * 8, 0)
+    w["permute"] = (R * 16, 0)
+    w["gate_up"] = (touched * 2 * mx(I, L) + R * L * 2 + R * I * act_b, 4 * R * I * L)
+    w["expert_down"] = (touched * mx(L, I) + R * I * act_b + R * L * act_b, 2 * R * L * I)
+    w["combine_norm"] = (R * L * act_b + T * L * 2, 0)
+    w["up_proj"] = (H * L * 2 + T * L * 2 + T * H * 4, 2 * T * H * L)
+    w["shared"] = ((2 * mx(S, H) + mx(H, S) + T * H * 2 + T * H * 4) if S else 0, 6 * T * S * H)
+    w["finish"] = (T * H * 6, 0)
+    w["prep"] = (R * L * 4, 0)
+    return w
+
+
+def expert_bytes(cfg):
+    mx = lambda rows, cols: rows * cols // 2 + rows * cols // 32
+    return 2 * mx(cfg.I, cfg.L) + mx(cfg.L, cfg.I)
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample_time(cfg, n_tokens, seed=0):
+    """Time the fp64 oracle on a fixed token sample; returns (seconds, tokens, threads)."""
+    import numpy as np
+    from latent_moe_layer_gb300 import synth
+    from oracle import oracle
+    rng = np.random.default_rng(1234 + seed)
+    rows = np.sort(rng.choice(cfg.T, min(n_tokens, cfg.T), replace=False))
+    x = synth.gen_x(cfg, rows)
+    dense = synth.gen_dense(cfg)
+    idx, _, _, _ = oracle.route(cfg, dense, x)
+    experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+    t0 = time.perf_counter()
+    oracle.forward(cfg, dense, experts, x)
+    dt = time.perf_counter() - t0
+    return dt, len(rows), oracle.max_threads()
+
+
+def cpu_sample_size(config_id):
+    return {0: 8, 1: 16, 2: 8, 3: 4, 4: 4}.get(config_id, 4)
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def reduce_max(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import __graft_entry__ as ge
+    from latent_moe_layer_gb300 import k3moe, synth
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    ge.build()
+    cfg = synth.CONFIGS[args.config]
+    pk, pk_src = peaks()
+
+    dw = k3moe.DeviceWeights(cfg)
+    layer = k3moe.Layer(cfg, path=args.path)
+    layer.load(dw)
+    path_tensor = layer.path_for(cfg.T) == k3moe.PATH_TENSOR
+    x = synth.gen_x(cfg)
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    out = torch.empty_like(xd)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    ws = layer.workspace(cfg.T)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        layer.forward(xd, out=out, idx_out=idx, w_out=wts, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError("device status after warm-up: %d" % layer.status())
+    touched = int(np.unique(idx.cpu().numpy()).size)
+
+    layer.profile(True)
+    layer.profile_read()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    nfw, stage_ms, stage_launch = layer.profile_read()
+    layer.profile(False)
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    total_ms = reduce_max(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = world * cfg.T * args.steps / (total_ms / 1e3)
+
+    # roofline of the dominant stage
+    work = stage_work(cfg, touched, path_tensor)
+    dom = max(stage_ms, key=lambda s: stage_ms[s])
+    per_launch_ms = stage_ms[dom] / max(1, nfw)
+    b, f = work[dom]
+    decode = cfg.T <= 256
+    if decode or f == 0:
+        ach = b / (per_launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None}
+    else:
+        ach = f / (per_launch_ms / 1e3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": None}
+    roof.update({"kernel_stage": dom, "per_launch_ms": round(per_launch_ms, 4),
+                 "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": pk_src})
+
+    # end to end through the host-buffer C-ABI call
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        for _ in range(2):
+            layer.forward_host(xh, oh, workspace=ws)
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            ee[i][0].record()
+            layer.forward_host(xh, oh, workspace=ws)
+            ee[i][1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ee), world)
+        e2e = {"value": round(world * cfg.T * args.steps / (e_ms / 1e3), 2), "unit": "tokens/s",
+               "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2,
+               "ms_per_step": round(e_ms / args.steps, 4)}
+
+    # CPU baseline: the oracle on a bounded token sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = cpu_sample_size(args.config)
+        dt, nt, thr = oracle_sample_time(cfg, n)
+        cpu = {"value": round(nt / dt, 4), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": f"{nt} tokens of {cfg.name} (fp64 oracle, all layer steps), {dt:.2f} s"}
+
+    exp_ms = stage_ms["gate_up"] + stage_ms["expert_down"]
+    detail = {
+        "stage_ms_per_step": {k: round(v / max(1, nfw), 4) for k, v in stage_ms.items() if v > 0},
+        "touched_experts": touched,
+        "expert_weight_gbs": round(touched * expert_bytes(cfg) / (exp_ms / max(1, nfw) / 1e3) / 1e9, 1)
+        if exp_ms > 0 else None,
+        "layer_tflops": round(sum(v[1] for v in work.values()) / (ms_step / 1e3) / 1e12, 3),
+        "path": "tensor" if path_tensor else "generic",
+    }
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if path_tensor else "f32", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
+                   "l2": "flushed between steps (512 MB write, outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "weights": "MXFP4 experts (E2M1 + E8M0/32), BF16 dense, seeded synthetic"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(sum(stage_launch.values())), "clocks": clk, "detail": detail,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from latent_moe_layer_gb300 import synth
+    from oracle import oracle
+    import numpy as np
+    oracle.build()
+    cfg = synth.CONFIGS[args.config]
+    n = {1: 2, 2: 2, 3: 1, 4: 1}.get(args.config, 1)
+    rng = np.random.default_rng(99)
+    dense = synth.gen_dense(cfg)
+    samples = []
+    for s in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(cfg.T, n, replace=False))
+        x = synth.gen_x(cfg, rows)
+        idx, _, _, _ = oracle.route(cfg, dense, x)
+        experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+        t0 = time.perf_counter()
+        oracle.forward(cfg, dense, experts, x)
+        samples.append(time.perf_counter() - t0)
+    timed = samples[args.warmup:]
+    tot = sum(timed)
+    val = n * args.steps / tot
+    thr = oracle.max_threads()
+    cpu = {"value": round(val, 4), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+           "sample": f"{n} random tokens of {cfg.name} per step (fp64 oracle, all layer steps)"}
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "tokens_per_step": n},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(val, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

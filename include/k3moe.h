@@ -1,0 +1,212 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) forward of the Kimi K3 latent
+ * routed-MoE layer.
+ *
+ * The layer (sources: "Kimi K3, as released", sections "The headline
+ * correction", "Shape" and "Against the technical report"; the K3 review's
+ * "Stable LatentMoE" section and parameter count; the GGUF notes' tensor
+ * inventory) computes, for every token x (hidden width H):
+ *
+ *   l = W_router x                      router logits, fp32-accurate
+ *   s = sigmoid(l); key = l, or s + b   b = e_score_correction_bias (selection only)
+ *   sel = top-K experts by key (descending; equal keys: lower expert index first)
+ *   w_k = s_k / sum_sel s * routed_scaling
+ *   h = W_down x                        routed_expert_down_proj, H -> L (latent)
+ *   y_e = W2_e (silu(W1_e h) * W3_e h)  GLU expert on the latent, MXFP4 weights
+ *   z = sum_k w_k y_{sel_k}
+ *   n = z / sqrt(mean(z^2) + eps) * gamma   routed_expert_norm (RMSNorm)
+ *   out = W_up n  [+ W2s (silu(W1s x) * W3s x)]   up_proj L -> H, optional shared GLU
+ *
+ * Conventions for every call:
+ *   - Return value: K3MOE_OK (0) or a negative K3MOE_ERR_* code; no exception
+ *     or abort crosses the ABI.  k3moe_strerror() names a code.
+ *   - Memory: every device buffer (weights, activations, outputs, workspaces)
+ *     is allocated and owned by the caller; the library borrows it for the
+ *     duration stated per call.  The library itself allocates only the host
+ *     handle.  Matrices are row-major ("out x in" for weights, as in the
+ *     checkpoint's shard header).
+ *   - Streams: device work is enqueued on the caller's stream and is
+ *     asynchronous unless a call says otherwise.  One handle serves one stream
+ *     at a time.  Device-side failures (bounded-wait timeouts, out-of-range
+ *     expert indices, f16 overflow of the GLU activation) are recorded in a
+ *     status word read by k3moe_status().
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ error codes */
+#define K3MOE_OK                 0
+#define K3MOE_ERR_ARG           -1   /* NULL pointer, negative size, bad enum */
+#define K3MOE_ERR_SHAPE         -2   /* dimension not supported (e.g. not a multiple of 32) */
+#define K3MOE_ERR_ALIGN         -3   /* pointer alignment below the stated requirement */
+#define K3MOE_ERR_BAD_SCALE     -4   /* an E8M0 scale byte equals 255 (NaN) */
+#define K3MOE_ERR_ALIAS         -5   /* an output overlaps an input */
+#define K3MOE_ERR_WORKSPACE     -6   /* workspace missing or smaller than required */
+#define K3MOE_ERR_CUDA          -7   /* a CUDA runtime/driver call failed */
+#define K3MOE_ERR_TIMEOUT       -8   /* a device-side bounded wait ran out */
+#define K3MOE_ERR_UNSUPPORTED   -9   /* option not implemented for this shape/path */
+#define K3MOE_ERR_RANGE        -10   /* device saw an expert index outside [0, E) or an f16 overflow */
+#define K3MOE_ERR_STATE        -11   /* call out of order (e.g. forward before load_weights) */
+
+/* ------------------------------------------------------------ enums */
+#define K3MOE_ACT_SILU          0    /* act(g) = g * sigmoid(g) */
+
+#define K3MOE_ROUTER_F32        0    /* W_router stored fp32 (the K3 checkpoint's router) */
+#define K3MOE_ROUTER_BF16       1    /* W_router stored BF16 */
+
+#define K3MOE_PATH_AUTO         0    /* tensor-core path when the shape allows it, else generic */
+#define K3MOE_PATH_GENERIC      1    /* CUDA-core kernels only (any shape meeting the basic rules) */
+#define K3MOE_PATH_TENSOR       2    /* tcgen05/TMA kernels (requires 16-byte row alignment) */
+
+/* ------------------------------------------------------------ configuration */
+typedef struct k3moe_config {
+    int hidden;          /* H, e.g. 7168; multiple of 32 */
+    int latent;          /* L, e.g. 3584 (routed_expert_hidden_size); multiple of 32 */
+    int n_experts;       /* E, e.g. 896; 1..1024 */
+    int top_k;           /* K, e.g. 16; 1..min(E, 32) */
+    int inter;           /* I, routed expert intermediate, e.g. 3072; multiple of 32 */
+    int shared_inter;    /* S, merged shared-expert intermediate (2 x 3072 = 6144), 0 = none */
+    float rms_eps;       /* routed_expert_norm epsilon, e.g. 1e-6 */
+    float routed_scaling;/* routed_scaling_factor, 1.0 for K3 */
+    int act;             /* K3MOE_ACT_* */
+    int router_dtype;    /* K3MOE_ROUTER_* */
+    int has_select_bias; /* 1: key = sigmoid(l) + b, b given in k3moe_weights.select_bias */
+    int path;            /* K3MOE_PATH_* */
+} k3moe_config;
+
+/*
+ * Weights, all device pointers, borrowed from load_weights until destroy.
+ * MXFP4 matrices are given per expert exactly as the checkpoint's shard header
+ * stores them: weight_packed U8 [rows, cols/2] (two E2M1 codes per byte, low
+ * nibble = lower column) and weight_scale U8 [rows, cols/32] (E8M0, value
+ * 2^(e-127)).  The per-expert arrays below are HOST arrays of n_experts device
+ * pointers (copied at load; the host arrays need not outlive the call).
+ *   w1 = gate [I, L], w3 = up [I, L], w2 = down [L, I]
+ *   ws1 = shared gate [S, H], ws3 = shared up [S, H], ws2 = shared down [H, S]
+ */
+typedef struct k3moe_weights {
+    const void *w_router;          /* [E, H] fp32 or BF16 (router_dtype) */
+    const float *select_bias;      /* [E] fp32, or NULL when has_select_bias == 0 */
+    const uint16_t *w_down;        /* [L, H] BF16 (routed_expert_down_proj) */
+    const uint16_t *w_up;          /* [H, L] BF16 (routed_expert_up_proj) */
+    const uint16_t *norm_gamma;    /* [L] BF16 (routed_expert_norm weight) */
+    const uint8_t *const *w1_packed, *const *w1_scale;
+    const uint8_t *const *w3_packed, *const *w3_scale;
+    const uint8_t *const *w2_packed, *const *w2_scale;
+    const uint8_t *ws1_packed, *ws1_scale;   /* shared experts; NULL when shared_inter == 0 */
+    const uint8_t *ws3_packed, *ws3_scale;
+    const uint8_t *ws2_packed, *ws2_scale;
+} k3moe_weights;
+
+typedef struct k3moe_handle k3moe_handle;
+
+/* Validate cfg and create a host handle (no device work).  *out is set only on success. */
+int k3moe_create(const k3moe_config *cfg, k3moe_handle **out);
+
+/* Bytes of caller-owned persistent device memory that load_weights needs
+ * (device copies of the expert pointer tables, TMA descriptors, the status
+ * word).  Valid after create. */
+size_t k3moe_persistent_bytes(const k3moe_handle *h);
+
+/*
+ * Check and record the weights.  `persistent` (>= k3moe_persistent_bytes,
+ * 256-byte aligned) must stay valid until destroy.  Scans every scale byte
+ * and fails with K3MOE_ERR_BAD_SCALE on a 255.  On the tensor path each
+ * packed/scale row must start 16-byte aligned (rows of the K3 shapes are
+ * 1792/1536/112/96 bytes, all multiples of 16) or the call fails with
+ * K3MOE_ERR_ALIGN.  Synchronises `stream` before returning.
+ */
+int k3moe_load_weights(k3moe_handle *h, const k3moe_weights *w, void *persistent,
+                       size_t persistent_bytes, cudaStream_t stream);
+
+/* Bytes of per-call device workspace for T tokens (256-byte aligned base),
+ * including the staging used by k3moe_forward_host. */
+size_t k3moe_workspace_bytes(const k3moe_handle *h, int T);
+
+/*
+ * Forward T >= 0 tokens.  x: [T, H] BF16 device; out: [T, H] BF16 device (must
+ * not overlap x: K3MOE_ERR_ALIAS).  idx_out [T, K] int32 and w_out [T, K] fp32
+ * (optional, may be NULL) receive the selected experts in selection order and
+ * their mixture weights.  T == 0 is a no-op.  Asynchronous on `stream`; the
+ * workspace must not be used by anything else until the stream reaches this
+ * point.
+ */
+int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx_out,
+                  float *w_out, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Same as k3moe_forward with HOST buffers (x_host [T,H] BF16, out_host [T,H]
+ * BF16, idx/w optional host arrays).  Copies in and out through the staging
+ * part of `workspace` on `stream` and synchronises before returning.  Host
+ * buffers should be pinned for full copy bandwidth.
+ */
+int k3moe_forward_host(k3moe_handle *h, const void *x_host, int T, void *out_host,
+                       int32_t *idx_host, float *w_host, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Synchronise `stream`, read and clear the device status word: K3MOE_OK or
+ * the first device-side error recorded since the last call. */
+int k3moe_status(k3moe_handle *h, cudaStream_t stream);
+
+/* Destroy the handle (host only; frees no caller memory).  NULL is allowed. */
+void k3moe_destroy(k3moe_handle *h);
+
+/* Static string for an error code. */
+const char *k3moe_strerror(int code);
+
+/* Which path k3moe_forward will take for T tokens: K3MOE_PATH_GENERIC or K3MOE_PATH_TENSOR. */
+int k3moe_path_for(const k3moe_handle *h, int T);
+
+/* ------------------------------------------------------------ profiling
+ * Stage timing with CUDA events recorded on the launching stream around each
+ * stage of k3moe_forward (a ring of 256 forwards), plus a count of kernel
+ * launches.  Off by default; enabling creates the events (host call). */
+#define K3MOE_STAGE_ROUTER      0   /* router logits (+ latent down-projection when fused) */
+#define K3MOE_STAGE_DOWN        1   /* routed_expert_down_proj */
+#define K3MOE_STAGE_TOPK        2
+#define K3MOE_STAGE_PERMUTE     3
+#define K3MOE_STAGE_GATE_UP     4   /* expert w1/w3 + activation */
+#define K3MOE_STAGE_EXPERT_DOWN 5   /* expert w2 */
+#define K3MOE_STAGE_COMBINE     6   /* combine + RMSNorm */
+#define K3MOE_STAGE_UP          7   /* routed_expert_up_proj */
+#define K3MOE_STAGE_SHARED      8   /* shared experts */
+#define K3MOE_STAGE_FINISH      9   /* output conversion */
+#define K3MOE_STAGE_PREP       10   /* activation conversion for the tensor path */
+#define K3MOE_NUM_STAGES       11
+
+int k3moe_profile_enable(k3moe_handle *h, int enable);
+/* Synchronise `stream`, then write per-stage milliseconds summed over the
+ * forwards recorded since the last read (stage_ms[K3MOE_NUM_STAGES]) and the
+ * number of kernel launches per stage (stage_launches, optional); returns the
+ * number of forwards covered (>= 0) or an error code.  Resets the ring. */
+int k3moe_profile_read(k3moe_handle *h, float *stage_ms, int *stage_launches, cudaStream_t stream);
+const char *k3moe_stage_name(int stage);
+
+/* ------------------------------------------------------------ test hooks
+ * Entry points that expose one device routine each, for unit tests.  They
+ * follow the conventions above. */
+
+/* Decode an MXFP4 matrix [rows, cols] (packed [rows, cols/2], scale
+ * [rows, cols/32], device) into fp32 out [rows, cols] with the device decoder
+ * the kernels use. */
+int k3moe_debug_dequant(const uint8_t *packed, const uint8_t *scale, int rows, int cols,
+                        float *out, cudaStream_t stream);
+
+/* Launch one CTA that waits on an mbarrier nothing ever arrives on, with the
+ * same bounded-wait helper as the pipelined kernels and `spin_limit`
+ * iterations.  The kernel gives up, records K3MOE_ERR_TIMEOUT in the handle's
+ * status word and returns; read it with k3moe_status(). */
+int k3moe_debug_wait_timeout(k3moe_handle *h, int spin_limit, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3MOE_H */

@@ -1,0 +1,397 @@
+// Generic CUDA-core kernels: any shape whose widths are multiples of 32.
+//
+//   rows_gemm     out[m, n] (+)= sum_k A[m, k] W[n, k]        (router, down/up projections)
+//   glu_generic   act[r, i] = silu(W1_e[i] . in[tok(r)]) * (W3_e[i] . in[tok(r)])
+//   down_generic  y[r, o] (+)= W2_e[o] . act[r]
+//   combine_norm  n[t] = rmsnorm(sum_k w[t, k] y[row(t, k)]) * gamma
+//
+// MXFP4 decoding: "Kimi K3, as released", Gate 3 section (two E2M1 codes per
+// byte, low nibble first; one E8M0 exponent per 32 weights, value 2^(e-127)).
+#include "k3moe_internal.h"
+#include "ptx.cuh"
+
+namespace k3 {
+
+// ------------------------------------------------------------------ dense rows GEMM
+// CTA: 8 warps x 2 W-rows = 16 output columns; TM tokens per CTA; A staged in
+// shared memory as fp32 in K-chunks of KC.
+constexpr int RG_TM = 16, RG_KC = 512, RG_ROWS = 16;
+
+template <bool A_BF16, bool W_BF16>
+__global__ void __launch_bounds__(256) rows_gemm_kernel(const void *__restrict__ Av, int M, int K,
+                                                        const void *__restrict__ Wv, int N,
+                                                        float *__restrict__ out32,
+                                                        uint16_t *__restrict__ out16, int accumulate)
+{
+    __shared__ __align__(16) float sA[RG_TM][RG_KC];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m0 = blockIdx.y * RG_TM;
+    const int n0 = blockIdx.x * RG_ROWS + warp * 2;
+    float acc[2][RG_TM];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int t = 0; t < RG_TM; ++t) acc[r][t] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += RG_KC) {
+        __syncthreads();
+        for (int i = tid; i < RG_TM * RG_KC; i += 256) {
+            int t = i / RG_KC, k = i % RG_KC;
+            float v = 0.f;
+            if (m0 + t < M && k0 + k < K) {
+                size_t o = (size_t)(m0 + t) * K + k0 + k;
+                v = A_BF16 ? bf16_to_f32(reinterpret_cast<const uint16_t *>(Av)[o])
+                           : reinterpret_cast<const float *>(Av)[o];
+            }
+            sA[t][k] = v;
+        }
+        __syncthreads();
+        float wv[2][4][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                int k = k0 + s * 128 + lane * 4;
+                int n = n0 + r;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wv[r][s][q] = 0.f;
+                if (n < N && k < K) {   // K is a multiple of 32, so k..k+3 are in range together
+                    size_t o = (size_t)n * K + k;
+                    if (W_BF16) {
+                        uint2 p = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(Wv) + o);
+                        wv[r][s][0] = __uint_as_float(p.x << 16);
+                        wv[r][s][1] = __uint_as_float(p.x & 0xffff0000u);
+                        wv[r][s][2] = __uint_as_float(p.y << 16);
+                        wv[r][s][3] = __uint_as_float(p.y & 0xffff0000u);
+                    } else {
+                        float4 p = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(Wv) + o);
+                        wv[r][s][0] = p.x; wv[r][s][1] = p.y; wv[r][s][2] = p.z; wv[r][s][3] = p.w;
+                    }
+                }
+            }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+#pragma unroll
+            for (int t = 0; t < RG_TM; ++t) {
+                float4 a = *reinterpret_cast<const float4 *>(&sA[t][s * 128 + lane * 4]);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    acc[r][t] = fmaf(wv[r][s][0], a.x, acc[r][t]);
+                    acc[r][t] = fmaf(wv[r][s][1], a.y, acc[r][t]);
+                    acc[r][t] = fmaf(wv[r][s][2], a.z, acc[r][t]);
+                    acc[r][t] = fmaf(wv[r][s][3], a.w, acc[r][t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int t = 0; t < RG_TM; ++t) {
+            float v = acc[r][t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            acc[r][t] = v;
+        }
+    // lane t writes token t of both rows
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int t = 0; t < RG_TM; ++t)
+            if (lane == t && m0 + t < M && n0 + r < N) {
+                size_t o = (size_t)(m0 + t) * N + n0 + r;
+                float v = acc[r][t];
+                if (out32) out32[o] = accumulate ? out32[o] + v : v;
+                if (out16) out16[o] = f32_to_bf16(v);
+            }
+}
+
+// ------------------------------------------------------------------ MXFP4 GLU (generic)
+constexpr int GX_TOK = 8;
+
+// Decode the 32 values of one MX block (16 packed bytes at p, E8M0 byte e).
+__device__ __forceinline__ void decode_block(const uint8_t *p, uint32_t e, float (&v)[32])
+{
+    float s = e8m0_to_f32(e);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w = p[4 * q] | (p[4 * q + 1] << 8) | (p[4 * q + 2] << 16) | ((uint32_t)p[4 * q + 3] << 24);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * q + j] = e2m1_to_f32((w >> (4 * j)) & 0xFu, s);
+    }
+}
+
+// Grid (dint / 8, n_groups); warp w computes output row i = 8 * blockIdx.x + w for
+// every row r of the group, GX_TOK rows at a time; lanes split the K blocks.
+__global__ void __launch_bounds__(256) glu_generic_kernel(
+    const uint16_t *__restrict__ in, int din, const int32_t *__restrict__ row_token, int rows,
+    const uint8_t *const *__restrict__ w1p, const uint8_t *const *__restrict__ w1s,
+    const uint8_t *const *__restrict__ w3p, const uint8_t *const *__restrict__ w3s,
+    const int32_t *__restrict__ offsets, int dint, float *__restrict__ act)
+{
+    const int g = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i = blockIdx.x * 8 + warp;
+    const int r0 = offsets ? offsets[g] : 0;
+    const int r1 = offsets ? offsets[g + 1] : rows;
+    if (r0 >= r1 || i >= dint) return;
+    const uint8_t *p1 = w1p[g] + (size_t)i * (din / 2), *s1 = w1s[g] + (size_t)i * (din / 32);
+    const uint8_t *p3 = w3p[g] + (size_t)i * (din / 2), *s3 = w3s[g] + (size_t)i * (din / 32);
+    const int nblk = din / 32;
+    for (int rb = r0; rb < r1; rb += GX_TOK) {
+        const int nt = min(GX_TOK, r1 - rb);
+        float gacc[GX_TOK], uacc[GX_TOK];
+#pragma unroll
+        for (int t = 0; t < GX_TOK; ++t) gacc[t] = uacc[t] = 0.f;
+        for (int b = lane; b < nblk; b += 32) {
+            float v1[32], v3[32];
+            decode_block(p1 + 16 * b, s1[b], v1);
+            decode_block(p3 + 16 * b, s3[b], v3);
+#pragma unroll
+            for (int t = 0; t < GX_TOK; ++t) {
+                if (t < nt) {
+                    int tok = row_token ? row_token[rb + t] : rb + t;
+                    const uint16_t *hv = in + (size_t)tok * din + 32 * b;
+                    float ga = 0.f, ua = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float x = bf16_to_f32(hv[j]);
+                        ga = fmaf(v1[j], x, ga);
+                        ua = fmaf(v3[j], x, ua);
+                    }
+                    gacc[t] += ga;
+                    uacc[t] += ua;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < GX_TOK; ++t) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                gacc[t] += __shfl_xor_sync(0xffffffffu, gacc[t], off);
+                uacc[t] += __shfl_xor_sync(0xffffffffu, uacc[t], off);
+            }
+        }
+        if (lane < nt) {
+            float gv = 0.f, uv = 0.f;
+#pragma unroll
+            for (int t = 0; t < GX_TOK; ++t)
+                if (t == lane) { gv = gacc[t]; uv = uacc[t]; }
+            float sg = gv / (1.0f + expf(-gv));
+            act[(size_t)(rb + lane) * dint + i] = sg * uv;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) down_generic_kernel(
+    const float *__restrict__ act, int dint, int rows, const uint8_t *const *__restrict__ w2p,
+    const uint8_t *const *__restrict__ w2s, const int32_t *__restrict__ offsets, int dout,
+    float *__restrict__ y, int accumulate)
+{
+    const int g = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int o = blockIdx.x * 8 + warp;
+    const int r0 = offsets ? offsets[g] : 0;
+    const int r1 = offsets ? offsets[g + 1] : rows;
+    if (r0 >= r1 || o >= dout) return;
+    const uint8_t *p2 = w2p[g] + (size_t)o * (dint / 2), *s2 = w2s[g] + (size_t)o * (dint / 32);
+    const int nblk = dint / 32;
+    for (int rb = r0; rb < r1; rb += GX_TOK) {
+        const int nt = min(GX_TOK, r1 - rb);
+        float acc[GX_TOK];
+#pragma unroll
+        for (int t = 0; t < GX_TOK; ++t) acc[t] = 0.f;
+        for (int b = lane; b < nblk; b += 32) {
+            float v[32];
+            decode_block(p2 + 16 * b, s2[b], v);
+#pragma unroll
+            for (int t = 0; t < GX_TOK; ++t) {
+                if (t < nt) {
+                    const float *av = act + (size_t)(rb + t) * dint + 32 * b;
+                    float a = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) a = fmaf(v[j], av[j], a);
+                    acc[t] += a;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < GX_TOK; ++t)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+        if (lane < nt) {
+            float v = 0.f;
+#pragma unroll
+            for (int t = 0; t < GX_TOK; ++t)
+                if (t == lane) v = acc[t];
+            size_t off = (size_t)(rb + lane) * dout + o;
+            y[off] = accumulate ? y[off] + v : v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ combine + RMSNorm
+// One CTA per token; fixed k order (deterministic, no atomics).
+constexpr int CN_MAXV = 32;   // L <= 256 * 32
+
+__global__ void __launch_bounds__(256) combine_norm_kernel(
+    const void *__restrict__ yv, int y_bf16, const int32_t *__restrict__ row_of,
+    const float *__restrict__ wts, const uint16_t *__restrict__ gamma, int K, int L, float eps,
+    uint16_t *__restrict__ nrm)
+{
+    const int t = blockIdx.x, tid = threadIdx.x;
+    __shared__ float red[8];
+    __shared__ int rows[64];
+    __shared__ float ws_[64];
+    if (tid < K) {
+        rows[tid] = row_of[(size_t)t * K + tid];
+        ws_[tid] = wts[(size_t)t * K + tid];
+    }
+    __syncthreads();
+    float z[CN_MAXV];
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < CN_MAXV; ++q) {
+        int i = tid + 256 * q;
+        float acc = 0.f;
+        if (i < L) {
+            for (int k = 0; k < K; ++k) {
+                size_t o = (size_t)rows[k] * L + i;
+                float yv_ = y_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t *>(yv)[o])
+                                   : reinterpret_cast<const float *>(yv)[o];
+                acc = fmaf(ws_[k], yv_, acc);
+            }
+        }
+        z[q] = acc;
+        ss = fmaf(acc, acc, ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)L + eps);
+#pragma unroll
+    for (int q = 0; q < CN_MAXV; ++q) {
+        int i = tid + 256 * q;
+        if (i < L) nrm[(size_t)t * L + i] = f32_to_bf16(z[q] * inv * bf16_to_f32(gamma[i]));
+    }
+}
+
+__global__ void finish_kernel(const float *__restrict__ o32, size_t n, uint16_t *__restrict__ out)
+{
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = f32_to_bf16(o32[i]);
+}
+
+__global__ void dequant_debug_kernel(const uint8_t *__restrict__ packed,
+                                     const uint8_t *__restrict__ scale, int rows, int cols,
+                                     float *__restrict__ out)
+{
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)rows * cols) return;
+    int r = (int)(i / cols), k = (int)(i % cols);
+    uint8_t byte = packed[(size_t)r * (cols / 2) + k / 2];
+    uint32_t code = (k & 1) ? (byte >> 4) : (byte & 0xF);
+    out[i] = e2m1_to_f32(code, e8m0_to_f32(scale[(size_t)r * (cols / 32) + k / 32]));
+}
+
+// One CTA; thread 0 waits on a barrier nothing arrives on.
+__global__ void wait_debug_kernel(int *status, int spin_limit)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait(smem_u32(&bar), 0, (uint32_t)spin_limit))
+            set_status(status, K3MOE_ERR_TIMEOUT, 1);
+        else  // cannot complete; kept so the wait is not optimised away
+            set_status(status, K3MOE_ERR_STATE, 1);
+    }
+}
+
+}  // namespace k3
+
+using namespace k3;
+
+#define K3_LAUNCH_OK() (cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA)
+
+int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,
+                        float *out_f32, uint16_t *out_bf16, int accumulate, cudaStream_t st)
+{
+    if (M == 0) return K3MOE_OK;
+    dim3 grid((N + RG_ROWS - 1) / RG_ROWS, (M + RG_TM - 1) / RG_TM);
+    if (grid.y > 65535) return K3MOE_ERR_UNSUPPORTED;
+    if (a_bf16 && w_bf16) rows_gemm_kernel<true, true><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else if (a_bf16) rows_gemm_kernel<true, false><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else if (w_bf16) rows_gemm_kernel<false, true><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else rows_gemm_kernel<false, false><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token, int rows,
+                          const uint8_t *const *w1p, const uint8_t *const *w1s,
+                          const uint8_t *const *w3p, const uint8_t *const *w3s,
+                          const int32_t *offsets, int n_groups, int dint, float *act, int *status,
+                          cudaStream_t st)
+{
+    (void)status;
+    if (n_groups > 65535) return K3MOE_ERR_UNSUPPORTED;
+    dim3 grid((dint + 7) / 8, n_groups);
+    glu_generic_kernel<<<grid, 256, 0, st>>>(in, din, row_token, rows, w1p, w1s, w3p, w3s, offsets, dint, act);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_down_generic(const float *act, int dint, int rows, const uint8_t *const *w2p,
+                           const uint8_t *const *w2s, const int32_t *offsets, int n_groups,
+                           int dout, float *y, int accumulate, cudaStream_t st)
+{
+    if (n_groups > 65535) return K3MOE_ERR_UNSUPPORTED;
+    dim3 grid((dout + 7) / 8, n_groups);
+    down_generic_kernel<<<grid, 256, 0, st>>>(act, dint, rows, w2p, w2s, offsets, dout, y, accumulate);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_combine_norm(const void *y, int y_bf16, const int32_t *row_of, const float *wts,
+                           const uint16_t *gamma, int T, int K, int L, float eps, uint16_t *nrm,
+                           cudaStream_t st)
+{
+    if (T == 0) return K3MOE_OK;
+    if (L > 256 * CN_MAXV || K > 64) return K3MOE_ERR_UNSUPPORTED;
+    combine_norm_kernel<<<T, 256, 0, st>>>(y, y_bf16, row_of, wts, gamma, K, L, eps, nrm);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_finish(const float *o32, int n, uint16_t *out, cudaStream_t st)
+{
+    if (n == 0) return K3MOE_OK;
+    finish_kernel<<<(unsigned)(((size_t)n + 255) / 256), 256, 0, st>>>(o32, (size_t)n, out);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_dequant_debug(const uint8_t *packed, const uint8_t *scale, int rows, int cols,
+                            float *out, cudaStream_t st)
+{
+    size_t n = (size_t)rows * cols;
+    if (n == 0) return K3MOE_OK;
+    dequant_debug_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(packed, scale, rows, cols, out);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_wait_debug(int *status, int spin_limit, cudaStream_t st)
+{
+    wait_debug_kernel<<<1, 32, 0, st>>>(status, spin_limit < 1 ? 1 : spin_limit);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}

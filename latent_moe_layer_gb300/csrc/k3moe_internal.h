@@ -1,0 +1,175 @@
+// Internal declarations shared by the translation units of libk3moe.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "k3moe.h"
+
+#define K3_CUDA_TRY(expr)                                   \
+    do {                                                    \
+        cudaError_t e_ = (expr);                            \
+        if (e_ != cudaSuccess) return K3MOE_ERR_CUDA;       \
+    } while (0)
+
+namespace k3 {
+
+// Device status word layout (int32 slots in the persistent buffer).
+enum StatusSlot { ST_CODE = 0, ST_DETAIL = 1, ST_COUNT = 4 };
+
+// Shared-memory budget of one CTA on sm_103a (opt-in maximum).
+constexpr int kMaxSmem = 227 * 1024;
+
+// Record the first device-side error (atomicCAS from OK).
+__device__ __forceinline__ void set_status(int *status, int code, int detail)
+{
+    if (atomicCAS(status + ST_CODE, K3MOE_OK, code) == K3MOE_OK)
+        status[ST_DETAIL] = detail;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b)
+{
+    return __uint_as_float((uint32_t)b << 16);
+}
+
+// fp32 -> BF16 round to nearest even (finite inputs; NaN stays NaN).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// 2^(e-127) for an E8M0 byte e in [0, 254] (e = 0 gives the fp32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e)
+{
+    return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+}
+
+// One E2M1 code -> fp32 value times `scale`.  The three magnitude bits placed
+// at fp32 bits 22..24 give exactly E2M1 x 2^-126 (exponent field 0 yields the
+// subnormal 0 / 0.5 cases), which 2^126 brings back to the E2M1 value.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code, float scale)
+{
+    float mag = __uint_as_float((code & 7u) << 22) * 0x1p126f;
+    float v = mag * scale;
+    return (code & 8u) ? -v : v;
+}
+
+}  // namespace k3
+
+// Kernel-launch counter (per host thread), read around each forward stage.
+extern thread_local long g_k3_launches;
+inline void k3_note_launch(int n = 1) { g_k3_launches += n; }
+
+// Stage timing ring (k3moe_profile_enable / k3moe_profile_read).
+struct k3_prof {
+    static constexpr int RING = 256;
+    bool on = false;
+    cudaEvent_t ev[RING][K3MOE_NUM_STAGES][2];
+    bool used[RING][K3MOE_NUM_STAGES];
+    int pos = 0;
+    long launches[K3MOE_NUM_STAGES];
+};
+
+// --------------------------------------------------------------- host handle
+struct k3moe_handle {
+    k3moe_config cfg;
+    bool loaded = false;
+    bool aligned16 = false;            // all packed/scale rows 16-byte aligned (tensor path eligible)
+    int num_sms = 0;
+    int device = 0;
+    // borrowed weights
+    const void *w_router = nullptr;
+    const float *bias = nullptr;
+    const uint16_t *w_down = nullptr, *w_up = nullptr, *gamma = nullptr;
+    const uint8_t *shared[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    // persistent (caller-owned) device buffer
+    uint8_t *persist = nullptr;
+    size_t persist_bytes = 0;
+    int *d_status = nullptr;                   // int[ST_COUNT]
+    const uint8_t **d_eptr[6] = {};            // device tables [E] for w1p,w1s,w3p,w3s,w2p,w2s
+    const uint8_t **d_shtab = nullptr;         // device table [6]: shared ws1p,ws1s,ws3p,ws3s,ws2p,ws2s
+    void *d_tmaps = nullptr;                   // tensor-path TMA descriptors (CUtensorMap[])
+    size_t tmap_count = 0;
+    k3_prof *prof = nullptr;                   // stage timing, when enabled
+};
+
+// Stage bracket used by the forward orchestration.
+struct k3_stage {
+    k3moe_handle *h;
+    int s;
+    cudaStream_t st;
+    long l0;
+    k3_stage(k3moe_handle *h_, int s_, cudaStream_t st_) : h(h_), s(s_), st(st_), l0(g_k3_launches)
+    {
+        if (h->prof && h->prof->on && h->prof->pos < k3_prof::RING) {
+            cudaEventRecord(h->prof->ev[h->prof->pos][s][0], st);
+            h->prof->used[h->prof->pos][s] = true;
+        }
+    }
+    ~k3_stage()
+    {
+        if (h->prof && h->prof->on) {
+            if (h->prof->pos < k3_prof::RING) cudaEventRecord(h->prof->ev[h->prof->pos][s][1], st);
+            h->prof->launches[s] += g_k3_launches - l0;
+        }
+    }
+};
+
+// --------------------------------------------------------------- workspace
+struct k3_ws {
+    float *logits;        // [T, E] fp32
+    uint16_t *h;          // [T, L] BF16 latent
+    int32_t *idx;         // [T, K]
+    float *wts;           // [T, K]
+    int32_t *counts;      // [E]
+    int32_t *offsets;     // [E + 1]
+    int32_t *tok_of;      // [T*K] permuted row -> token
+    int32_t *row_of;      // [T*K] (t, k) -> permuted row
+    int32_t *meta;        // small scalars: [0] = number of active experts, [1] = number of tiles
+    int32_t *active;      // [E] active expert list
+    int32_t *tiles;       // tensor-path tile list (int4 per tile)
+    void *act;            // [T*K, I] fp32 (generic) or f16 (tensor path)
+    void *y;              // [T*K, L] fp32 (generic) or BF16 (tensor path)
+    void *hperm;          // [T*K, L] f16 (tensor path) activation rows in expert order
+    float *hscale;        // [T*K] per-row power-of-two factor of hperm
+    uint16_t *nrm;        // [T, L] BF16 normalised latent
+    float *o32;           // [T, H] fp32 up_proj (+ shared) accumulator
+    void *sact;           // [T, S] shared-expert activation (fp32 generic / f16 tensor)
+    void *xs;             // [T, H] f16 scaled copy of x for the shared GLU (tensor path)
+    float *xscale;        // [T]
+    uint16_t *stage_x;    // [T, H] BF16 staging for k3moe_forward_host
+    uint16_t *stage_out;  // [T, H]
+    int32_t *stage_idx;   // [T, K]
+    float *stage_w;       // [T, K]
+    size_t bytes;
+};
+
+int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base may be NULL (sizing)
+
+// --------------------------------------------------------------- launchers
+// routing and permutation (route.cu)
+int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
+                   cudaStream_t st);
+int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);
+
+// generic CUDA-core kernels (generic.cu)
+int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,
+                        float *out_f32, uint16_t *out_bf16, int accumulate, cudaStream_t st);
+int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token, int rows,
+                          const uint8_t *const *w1p, const uint8_t *const *w1s,
+                          const uint8_t *const *w3p, const uint8_t *const *w3s,
+                          const int32_t *offsets, int n_groups, int dint, float *act,
+                          int *status, cudaStream_t st);
+int k3_launch_down_generic(const float *act, int dint, int rows, const uint8_t *const *w2p,
+                           const uint8_t *const *w2s, const int32_t *offsets, int n_groups,
+                           int dout, float *y, int accumulate, cudaStream_t st);
+int k3_launch_combine_norm(const void *y, int y_bf16, const int32_t *row_of, const float *wts,
+                           const uint16_t *gamma, int T, int K, int L, float eps, uint16_t *nrm,
+                           cudaStream_t st);
+int k3_launch_finish(const float *o32, int n, uint16_t *out, cudaStream_t st);
+int k3_launch_dequant_debug(const uint8_t *packed, const uint8_t *scale, int rows, int cols,
+                            float *out, cudaStream_t st);
+int k3_launch_wait_debug(int *status, int spin_limit, cudaStream_t st);

@@ -1,0 +1,222 @@
+// Router top-K selection and the counting-sort token permutation.
+//
+// Selection ("Kimi K3, as released", table "Shape": sigmoid router, 1 group,
+// routed_scaling_factor 1.0; section "Against the technical report":
+// e_score_correction_bias for selection only, weights renormalised over the
+// selected top-k, then routed_scaling_factor).  Permutation: rows grouped per
+// expert so the gate/up and down GEMMs read the same per-expert row ranges
+// ("quants.md", the moe_align_block_size fix: one layout shared by both GEMMs,
+// expert ids >= 256 kept; indices here are int32).
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+// One warp per token.  Lane l holds keys j = l + 32 i.  Each of the K rounds
+// takes the warp-wide maximum key, lower index first on equal keys; NaN keys
+// rank below every number.  Writes idx in selection order and the mixture
+// weights sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
+template <int MAXP>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits,
+                                                   const float *__restrict__ bias, int T, int E,
+                                                   int K, float scaling, int32_t *__restrict__ idx,
+                                                   float *__restrict__ wts)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const float *lrow = logits + (size_t)warp * E;
+    float key[MAXP];
+#pragma unroll
+    for (int i = 0; i < MAXP; ++i) {
+        int j = lane + 32 * i;
+        float k = -INFINITY;
+        if (j < E) {
+            float l = lrow[j];
+            if (bias) k = 1.0f / (1.0f + expf(-l)) + bias[j];
+            else k = l;
+            if (k != k) k = -INFINITY;
+        }
+        key[i] = k;
+    }
+    uint32_t taken = 0;
+    int mine = -1;            // selection slot this lane writes (lane s writes slot s)
+    float ssum = 0.f;
+    int sel_j = 0;
+    for (int s = 0; s < K; ++s) {
+        float bk = -INFINITY;
+        int bj = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < MAXP; ++i) {
+            int j = lane + 32 * i;
+            bool free_ = !((taken >> i) & 1u) && j < E;
+            if (free_ && (key[i] > bk || (key[i] == bk && j < bj))) {
+                bk = key[i];
+                bj = j;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+            int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+            if (ok > bk || (ok == bk && oj < bj)) {
+                bk = ok;
+                bj = oj;
+            }
+        }
+        if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
+        float l = lrow[bj];
+        float sg = 1.0f / (1.0f + expf(-l));
+        ssum += sg;
+        if (lane == s) {
+            mine = s;
+            sel_j = bj;
+        }
+    }
+    if (mine >= 0) {
+        float l = lrow[sel_j];
+        float sg = 1.0f / (1.0f + expf(-l));
+        idx[(size_t)warp * K + mine] = sel_j;
+        wts[(size_t)warp * K + mine] = sg / ssum * scaling;
+    }
+}
+
+// counts[e] = number of (t, k) selecting e; flags an index outside [0, E).
+__global__ void perm_count_kernel(const int32_t *__restrict__ idx, int n, int E,
+                                  int32_t *__restrict__ counts, int *status)
+{
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    int e = idx[i];
+    if (e < 0 || e >= E) {
+        set_status(status, K3MOE_ERR_RANGE, e);
+        return;
+    }
+    atomicAdd(counts + e, 1);
+}
+
+// Single CTA: offsets = exclusive scan of counts; active-expert list; tile list
+// for the tensor path (expert, first row, rows) with at most tile_n rows each.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restrict__ counts, int E,
+                                                         int tile_n, int32_t *__restrict__ offsets,
+                                                         int32_t *__restrict__ active,
+                                                         int4 *__restrict__ tiles,
+                                                         int32_t *__restrict__ meta)
+{
+    __shared__ int s_cnt[1024], s_act[1024], s_til[1024];
+    __shared__ int base_rows, base_act, base_til;
+    const int tid = threadIdx.x;
+    if (tid == 0) base_rows = base_act = base_til = 0;
+    __syncthreads();
+    for (int e0 = 0; e0 < E; e0 += 1024) {
+        int e = e0 + tid;
+        int c = e < E ? counts[e] : 0;
+        int nt = (tile_n > 0) ? (c + tile_n - 1) / tile_n : 0;
+        s_cnt[tid] = c;
+        s_act[tid] = c > 0;
+        s_til[tid] = nt;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {     // inclusive Hillis-Steele scans
+            int a = tid >= off ? s_cnt[tid - off] : 0;
+            int b = tid >= off ? s_act[tid - off] : 0;
+            int d = tid >= off ? s_til[tid - off] : 0;
+            __syncthreads();
+            s_cnt[tid] += a;
+            s_act[tid] += b;
+            s_til[tid] += d;
+            __syncthreads();
+        }
+        if (e < E) {
+            int row0 = base_rows + s_cnt[tid] - c;
+            offsets[e] = row0;
+            if (c > 0) active[base_act + s_act[tid] - 1] = e;
+            int t0 = base_til + s_til[tid] - nt;
+            for (int q = 0; q < nt; ++q) {
+                int r = q * tile_n;
+                tiles[t0 + q] = make_int4(e, row0 + r, min(tile_n, c - r), 0);
+            }
+        }
+        __syncthreads();
+        if (tid == 1023) {
+            base_rows += s_cnt[1023];
+            base_act += s_act[1023];
+            base_til += s_til[1023];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        offsets[E] = base_rows;
+        meta[0] = base_act;
+        meta[1] = base_til;
+    }
+}
+
+// One CTA per expert: stable scatter of its (t, k) pairs in (t, k) order.
+__global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t *__restrict__ idx, int n,
+                                                           int K, const int32_t *__restrict__ counts,
+                                                           const int32_t *__restrict__ offsets,
+                                                           int32_t *__restrict__ tok_of,
+                                                           int32_t *__restrict__ row_of)
+{
+    const int e = blockIdx.x;
+    if (counts[e] == 0) return;
+    __shared__ int warp_tot[8];
+    __shared__ int base;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) base = offsets[e];
+    __syncthreads();
+    for (int p0 = 0; p0 < n; p0 += 256) {
+        int p = p0 + tid;
+        bool hit = p < n && idx[p] == e;
+        uint32_t bal = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0) warp_tot[w] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            before += q < w ? warp_tot[q] : 0;
+            total += warp_tot[q];
+        }
+        if (hit) {
+            int row = base + before + __popc(bal & ((1u << lane) - 1u));
+            tok_of[row] = p / K;
+            row_of[p] = row;
+        }
+        __syncthreads();
+        if (tid == 0) base += total;
+        __syncthreads();
+    }
+}
+
+}  // namespace k3
+
+using namespace k3;
+
+int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
+                   cudaStream_t st)
+{
+    const k3moe_config &c = h->cfg;
+    const float *bias = c.has_select_bias ? h->bias : nullptr;
+    dim3 grid((T + 7) / 8), block(256);
+    int E = c.n_experts;
+    if (E <= 128) topk_kernel<4><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
+    else if (E <= 256) topk_kernel<8><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
+    else if (E <= 512) topk_kernel<16><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
+    else if (E <= 1024) topk_kernel<32><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
+    else return K3MOE_ERR_UNSUPPORTED;
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)
+{
+    const int E = h->cfg.n_experts, K = h->cfg.top_k, n = T * K;
+    K3_CUDA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int32_t) * E, st));
+    perm_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(ws.idx, n, E, ws.counts, h->d_status);
+    k3_note_launch();
+    perm_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, E, tile_n, ws.offsets, ws.active,
+                                         reinterpret_cast<int4 *>(ws.tiles), ws.meta);
+    k3_note_launch();
+    perm_scatter_kernel<<<E, 256, 0, st>>>(ws.idx, n, K, ws.counts, ws.offsets, ws.tok_of, ws.row_of);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}

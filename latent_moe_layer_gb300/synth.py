@@ -88,6 +88,11 @@ CONFIGS = {
                    select_bias=True, **K3),
 }
 
+# A small shape whose packed/scale rows are 16-byte aligned (the tensor-core
+# path's requirement) and that spans several 128-row tiles with a ragged tail.
+SMALL_ALIGNED = LayerConfig("small_aligned_t40", seed=10, wseed=10, T=40, H=1024, L=512, E=24,
+                            K=4, I=640, exp_lo=118, exp_hi=122)
+
 
 # ---------------------------------------------------------------- helpers
 def _rng(*key: int) -> np.random.Generator:

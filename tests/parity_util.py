@@ -1,0 +1,95 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI,
+run the oracle on the same seeded inputs, compare.
+
+Tolerances (the layer's stated bar): expert indices identical as sets wherever
+the K-th/(K+1)-th key gap is >= 1e-4 (near-ties counted, not compared);
+relative L2 <= 2e-2 and max-abs <= 5e-2 on the output, the max-abs taken on the
+output divided by the oracle output's RMS when that RMS exceeds 1 (the shared
+experts of the skewed prefill case lift the output scale to ~40, where the
+BF16 output's own half-ulp is 0.25); mixture weights within 1e-5.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from latent_moe_layer_gb300 import synth
+from oracle import oracle
+
+REL_L2 = 2e-2
+MAX_ABS = 5e-2
+GAP = 1e-4
+W_TOL = 1e-5
+
+_WEIGHTS = {}
+
+
+def device_weights(cfg):
+    """DeviceWeights for cfg, cached per weight seed and shape (one set at a time)."""
+    from latent_moe_layer_gb300 import k3moe
+    key = (cfg.wseed, cfg.H, cfg.L, cfg.E, cfg.I, cfg.S, cfg.exp_lo, cfg.exp_hi, cfg.router_dtype,
+           cfg.select_bias)
+    if key not in _WEIGHTS:
+        _WEIGHTS.clear()
+        import torch
+        torch.cuda.empty_cache()
+        _WEIGHTS[key] = k3moe.DeviceWeights(cfg)
+    return _WEIGHTS[key]
+
+
+def run_gpu(cfg, path, x=None, dw=None):
+    import torch
+    from latent_moe_layer_gb300 import k3moe
+    dw = dw if dw is not None else device_weights(cfg)
+    layer = k3moe.Layer(cfg, path=path)
+    layer.load(dw)
+    x = synth.gen_x(cfg) if x is None else x
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    T = x.shape[0]
+    idx = torch.empty((T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
+    out = layer.forward(xd, idx_out=idx, w_out=w)
+    torch.cuda.synchronize()
+    st = layer.status()
+    res = dict(out=synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64),
+               idx=idx.cpu().numpy(), w=w.cpu().numpy().astype(np.float64), status=st,
+               path=layer.path_for(T), x=x)
+    del layer
+    return res
+
+
+def oracle_rows(cfg, dense, x_rows, nthreads=0):
+    idx, _, _, _ = oracle.route(cfg, dense, x_rows, nthreads=nthreads)
+    experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+    return oracle.forward(cfg, dense, experts, x_rows, nthreads=nthreads)
+
+
+def compare(cfg, gpu, ref, rows=None):
+    """Compare GPU results (all T tokens) with the oracle on `rows` (default all)."""
+    rows = np.arange(gpu["out"].shape[0]) if rows is None else np.asarray(rows)
+    g_out, g_idx, g_w = gpu["out"][rows], gpu["idx"][rows], gpu["w"][rows]
+    r_out = ref["out"]
+    err = g_out - r_out
+    rel = float(np.linalg.norm(err) / np.linalg.norm(r_out))
+    rms = float(np.sqrt((r_out ** 2).mean()))
+    mx = float(np.abs(err).max() / max(rms, 1.0))
+    sel = ref["gap"] >= GAP
+    near = int((~sel).sum())
+    idx_bad = [int(t) for t in np.nonzero(sel)[0]
+               if set(g_idx[t].tolist()) != set(ref["idx"][t].tolist())]
+    order_bad = 0
+    w_err = 0.0
+    for t in np.nonzero(sel)[0]:
+        if int(t) in idx_bad:
+            continue
+        pos = {int(e): k for k, e in enumerate(ref["idx"][t])}
+        for k, e in enumerate(g_idx[t]):
+            w_err = max(w_err, abs(g_w[t, k] - ref["w"][t, pos[int(e)]]))
+    return dict(rel_l2=rel, max_abs=mx, near_ties=near, idx_mismatch=len(idx_bad),
+                w_err=w_err, out_rms=rms, order_bad=order_bad)
+
+
+def assert_parity(m):
+    assert m["idx_mismatch"] == 0, m
+    assert m["rel_l2"] <= REL_L2, m
+    assert m["max_abs"] <= MAX_ABS, m
+    assert m["w_err"] <= W_TOL, m

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output element; the K3-size cases compare index
+sets on every token (or a large sample) and outputs on sampled tokens the
+oracle computes one by one (tokens are independent, so a sample is exact for
+those tokens).
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+from latent_moe_layer_gb300 import synth
+from oracle import oracle
+
+from parity_util import assert_parity, compare, device_weights, oracle_rows, run_gpu
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from latent_moe_layer_gb300 import k3moe  # noqa: E402
+
+GEN, TEN, AUTO = k3moe.PATH_GENERIC, k3moe.PATH_TENSOR, k3moe.PATH_AUTO
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+# ------------------------------------------------------------------ device decoder
+def test_debug_dequant_every_byte_and_exponent():
+    rows = 64
+    packed = np.tile(np.arange(256, dtype=np.uint8), (rows, 1))          # 512 values per row
+    scale = (np.arange(rows * 16, dtype=np.int64).reshape(rows, 16) % 253).astype(np.uint8)  # 0..252
+    got = k3moe.debug_dequant(torch.from_numpy(packed).cuda(), torch.from_numpy(scale).cuda())
+    ref = oracle.dequant(packed, scale)
+    assert np.array_equal(got.cpu().numpy().astype(np.float64), ref)
+
+
+# ------------------------------------------------------------------ tiny / small shapes
+def test_tiny_t8_full_parity():
+    cfg = synth.CONFIGS[0]
+    g = run_gpu(cfg, AUTO)
+    assert g["status"] == 0 and g["path"] == GEN
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 100, 333])
+def test_tiny_ragged_token_counts(T):
+    cfg = synth.CONFIGS[0].with_tokens(T)
+    g = run_gpu(cfg, GEN)
+    assert g["status"] == 0
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
+@pytest.mark.parametrize("path", [GEN])
+def test_small_aligned_parity(path):
+    cfg = synth.SMALL_ALIGNED
+    g = run_gpu(cfg, path)
+    assert g["status"] == 0
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
+def test_batch_invariance():
+    cfg = synth.SMALL_ALIGNED.with_tokens(37)
+    full = run_gpu(cfg, AUTO)
+    x = full["x"]
+    for t in [0, 13, 36]:
+        one = run_gpu(cfg.with_tokens(1), AUTO, x=x[t:t + 1])
+        np.testing.assert_array_equal(one["out"][0], full["out"][t])
+        np.testing.assert_array_equal(one["idx"][0], full["idx"][t])
+
+
+def test_equal_logits_pick_lowest_indices():
+    cfg = synth.CONFIGS[0]
+    dw = k3moe.DeviceWeights(cfg)
+    dw.w_router.copy_(dw.w_router[:1].expand_as(dw.w_router).clone())
+    g = run_gpu(cfg, AUTO, dw=dw)
+    assert np.all(g["idx"] == np.arange(cfg.K))
+    np.testing.assert_allclose(g["w"], 1.0 / cfg.K, rtol=1e-6)
+
+
+def test_selection_bias_routes_but_does_not_weight():
+    base = synth.CONFIGS[0]
+    cfg = synth.LayerConfig(**{**base.__dict__, "select_bias": True, "name": "tiny_bias"})
+    dense = synth.gen_dense(base)
+    dense.select_bias = np.random.default_rng(9).uniform(-0.3, 0.3, cfg.E).astype(np.float32)
+    dw = k3moe.DeviceWeights(cfg, dense=dense)
+    g = run_gpu(cfg, AUTO, dw=dw)
+    ref = oracle_rows(cfg, dense, g["x"])
+    m = compare(cfg, g, ref)
+    assert_parity(m)
+
+
+def test_forward_host_matches_device():
+    cfg = synth.SMALL_ALIGNED
+    dw = device_weights(cfg)
+    layer = k3moe.Layer(cfg)
+    layer.load(dw)
+    x = synth.gen_x(cfg)
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    out_d = layer.forward(xd)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    out_h = torch.empty_like(xh).pin_memory()
+    idx_h = torch.empty((cfg.T, cfg.K), dtype=torch.int32).pin_memory()
+    layer.forward_host(xh, out_h, idx_host=idx_h)
+    assert torch.equal(out_h, out_d.cpu())
+    assert idx_h.min() >= 0 and idx_h.max() < cfg.E
+
+
+# ------------------------------------------------------------------ argument and state errors
+def test_errors_are_reported():
+    cfg = synth.CONFIGS[0]
+    dw = device_weights(cfg)
+    layer = k3moe.Layer(cfg)
+    layer.load(dw)
+    L = k3moe.lib()
+    x = torch.from_numpy(synth.gen_x(cfg).view(np.int16)).cuda()
+    ws = layer.workspace(cfg.T)
+    s = torch.cuda.current_stream().cuda_stream
+    # T = 0 is a no-op
+    assert L.k3moe_forward(layer.h, x.data_ptr(), 0, x.data_ptr(), None, None, ws.data_ptr(),
+                           ws.numel(), s) == 0
+    # out aliasing x
+    assert L.k3moe_forward(layer.h, x.data_ptr(), cfg.T, x.data_ptr(), None, None, ws.data_ptr(),
+                           ws.numel(), s) == k3moe.ERR_CODE["ALIAS"]
+    out = torch.empty_like(x)
+    assert L.k3moe_forward(layer.h, x.data_ptr(), cfg.T, out.data_ptr(), None, None, ws.data_ptr(),
+                           16, s) == k3moe.ERR_CODE["WORKSPACE"]
+    assert L.k3moe_forward(layer.h, x.data_ptr(), -1, out.data_ptr(), None, None, ws.data_ptr(),
+                           ws.numel(), s) == k3moe.ERR_CODE["ARG"]
+    assert L.k3moe_forward(layer.h, x.data_ptr() + 2, cfg.T, out.data_ptr(), None, None,
+                           ws.data_ptr(), ws.numel(), s) == k3moe.ERR_CODE["ALIGN"]
+    assert layer.status() == 0
+
+
+def test_nan_scale_rejected_at_load():
+    cfg = synth.CONFIGS[0]
+    dw = k3moe.DeviceWeights(cfg)
+    dw.scale[2][5, 3, 1] = 255
+    layer = k3moe.Layer(cfg)
+    with pytest.raises(k3moe.K3Error) as e:
+        layer.load(dw)
+    assert e.value.code == k3moe.ERR_CODE["BAD_SCALE"]
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    cfg = synth.CONFIGS[0]
+    dw = device_weights(cfg)
+    layer = k3moe.Layer(cfg)
+    layer.load(dw)
+    layer.debug_wait_timeout(1)
+    assert layer.status() == k3moe.ERR_CODE["TIMEOUT"]
+    assert layer.status() == 0                  # cleared by the read
+    g = run_gpu(cfg, AUTO, dw=dw)               # the context is still usable
+    assert g["status"] == 0
+
+
+# ------------------------------------------------------------------ K3 sizes
+def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0):
+    cfg = synth.CONFIGS[cfg_id]
+    dw = device_weights(cfg)
+    g = run_gpu(cfg, path, dw=dw)
+    assert g["status"] == 0
+    rng = np.random.default_rng(100 + seed)
+    T = cfg.T
+    r_rows = np.arange(T) if n_route >= T else np.sort(rng.choice(T, n_route, replace=False))
+    o_rows = r_rows if n_out >= len(r_rows) else np.sort(rng.choice(r_rows, n_out, replace=False))
+    idx, w, gap, _ = oracle.route(cfg, dw.dense, g["x"][r_rows])
+    bad = [i for i, t in enumerate(r_rows)
+           if gap[i] >= 1e-4 and set(g["idx"][t].tolist()) != set(idx[i].tolist())]
+    assert not bad, f"index mismatch on {len(bad)} tokens"
+    ref = oracle_rows(cfg, dw.dense, g["x"][o_rows])
+    m = compare(cfg, g, ref, rows=o_rows)
+    m["near_ties_routed"] = int((gap < 1e-4).sum())
+    print(cfg.name, m)
+    assert_parity(m)
+    return g, m
+
+
+def test_k3_decode_t16():
+    _k3_case(1, 16, 16)
+
+
+def test_k3_decode_t256():
+    _k3_case(2, 256, 48)
+
+
+def test_k3_prefill_t8192():
+    _k3_case(3, 512, 24)
+
+
+def test_k3_prefill_t32768_skew_shared():
+    g, m = _k3_case(4, 512, 16)
+    loads = np.bincount(g["idx"].ravel(), minlength=896)
+    assert (loads > 0).sum() < 100            # the Zipf selection bias concentrates the load
