@@ -64,6 +64,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
     const uint8_t **shtab = cv.take<const uint8_t *>(6);
     size_t ntm = k3_tc_tmap_count(c);
     void *tm = cv.take<uint8_t>(ntm * 128 + 128);
+    uint8_t *rmax = cv.take<uint8_t>(k3_tc_rowmax_bytes(c));
     int *flag = cv.take<int>(1);
     (void)flag;
     if (h) {
@@ -72,6 +73,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
         h->d_shtab = shtab;
         h->d_tmaps = base ? (void *)align_up((uintptr_t)tm, 128) : nullptr;
         h->tmap_count = ntm;
+        h->d_rowmax = rmax;
     }
     return align_up(cv.off, 256);
 }
@@ -220,14 +222,13 @@ int k3moe_load_weights(k3moe_handle *h, const k3moe_weights *w, void *persistent
             if (!sh[i]) return K3MOE_ERR_ARG;
 
     // 16-byte alignment of every packed/scale row (tensor path requirement)
-    bool al = (c.latent / 2) % 16 == 0 && (c.latent / 32) % 16 == 0 && (c.inter / 2) % 16 == 0 &&
-              (c.inter / 32) % 16 == 0 && (c.hidden % 64) == 0;
+    // (tensor path: K of every GEMM a multiple of 512 = 16-byte scale groups, rows a multiple of 128)
+    bool al = c.latent % 512 == 0 && c.inter % 512 == 0 && c.hidden % 128 == 0;
     for (int i = 0; i < 6 && al; ++i)
         for (int e = 0; e < c.n_experts; ++e)
             if ((uintptr_t)tabs[i][e] % 16) { al = false; break; }
     if (c.shared_inter > 0) {
-        al = al && (c.hidden / 2) % 16 == 0 && (c.hidden / 32) % 16 == 0 &&
-             (c.shared_inter / 2) % 16 == 0 && (c.shared_inter / 32) % 16 == 0;
+        al = al && c.hidden % 512 == 0 && c.shared_inter % 512 == 0;
         for (int i = 0; i < 6; ++i) al = al && ((uintptr_t)sh[i] % 16 == 0);
     }
     if (c.path == K3MOE_PATH_TENSOR && !al) return K3MOE_ERR_ALIGN;
@@ -280,7 +281,7 @@ int k3moe_path_for(const k3moe_handle *h, int T)
 {
     (void)T;
     if (!h) return K3MOE_ERR_ARG;
-    if (h->cfg.path == K3MOE_PATH_GENERIC || !h->aligned16) return K3MOE_PATH_GENERIC;
+    if (h->cfg.path == K3MOE_PATH_GENERIC || !h->aligned16 || !k3_tc_available()) return K3MOE_PATH_GENERIC;
     return K3MOE_PATH_TENSOR;
 }
 
@@ -394,8 +395,9 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
 
 extern "C" {
 
-int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx_out, float *w_out,
-                  void *workspace, size_t workspace_bytes, cudaStream_t st)
+static int forward_impl(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx_out,
+                        float *w_out, void *workspace, size_t workspace_bytes, cudaStream_t st,
+                        bool staged)
 {
     if (!h) return K3MOE_ERR_ARG;
     if (!h->loaded) return K3MOE_ERR_STATE;
@@ -403,16 +405,20 @@ int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx
     if (T == 0) return K3MOE_OK;
     if (!x || !out || !workspace) return K3MOE_ERR_ARG;
     const k3moe_config &c = h->cfg;
+    if ((uintptr_t)x % 16 || (uintptr_t)out % 16) return K3MOE_ERR_ALIGN;
+    if ((uintptr_t)workspace % 256) return K3MOE_ERR_ALIGN;
     const size_t xb = (size_t)T * c.hidden * 2;
     if (overlaps(x, xb, out, xb)) return K3MOE_ERR_ALIAS;
     if (idx_out && overlaps(x, xb, idx_out, (size_t)T * c.top_k * 4)) return K3MOE_ERR_ALIAS;
     if (w_out && overlaps(x, xb, w_out, (size_t)T * c.top_k * 4)) return K3MOE_ERR_ALIAS;
-    if ((uintptr_t)x % 16 || (uintptr_t)out % 16) return K3MOE_ERR_ALIGN;
-    if ((uintptr_t)workspace % 256) return K3MOE_ERR_ALIGN;
     k3_ws ws;
     k3_ws_layout(h, T, workspace, &ws);
     if (workspace_bytes < ws.bytes) return K3MOE_ERR_WORKSPACE;
-    if (overlaps(workspace, ws.bytes, x, xb) || overlaps(workspace, ws.bytes, out, xb))
+    // the compute part of the workspace ends where the host-call staging begins
+    const size_t compute_bytes = (size_t)((uint8_t *)ws.stage_x - (uint8_t *)workspace);
+    if (!staged && (overlaps(workspace, ws.bytes, x, xb) || overlaps(workspace, ws.bytes, out, xb)))
+        return K3MOE_ERR_ALIAS;
+    if (staged && (overlaps(workspace, compute_bytes, x, xb) || overlaps(workspace, compute_bytes, out, xb)))
         return K3MOE_ERR_ALIAS;
     int dev = 0;
     K3_CUDA_TRY(cudaGetDevice(&dev));
@@ -425,6 +431,12 @@ int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx
     if (idx_out) K3_CUDA_TRY(cudaMemcpyAsync(idx_out, ws.idx, kb, cudaMemcpyDeviceToDevice, st));
     if (w_out) K3_CUDA_TRY(cudaMemcpyAsync(w_out, ws.wts, kb, cudaMemcpyDeviceToDevice, st));
     return K3MOE_OK;
+}
+
+int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx_out, float *w_out,
+                  void *workspace, size_t workspace_bytes, cudaStream_t st)
+{
+    return forward_impl(h, x, T, out, idx_out, w_out, workspace, workspace_bytes, st, false);
 }
 
 int k3moe_forward_host(k3moe_handle *h, const void *x_host, int T, void *out_host, int32_t *idx_host,
@@ -442,8 +454,8 @@ int k3moe_forward_host(k3moe_handle *h, const void *x_host, int T, void *out_hos
     if (workspace_bytes < ws.bytes) return K3MOE_ERR_WORKSPACE;
     const size_t xb = (size_t)T * c.hidden * 2, kb = (size_t)T * c.top_k * 4;
     K3_CUDA_TRY(cudaMemcpyAsync(ws.stage_x, x_host, xb, cudaMemcpyHostToDevice, st));
-    int rc = k3moe_forward(h, ws.stage_x, T, ws.stage_out, idx_host ? ws.stage_idx : nullptr,
-                           w_host ? ws.stage_w : nullptr, workspace, workspace_bytes, st);
+    int rc = forward_impl(h, ws.stage_x, T, ws.stage_out, idx_host ? ws.stage_idx : nullptr,
+                          w_host ? ws.stage_w : nullptr, workspace, workspace_bytes, st, true);
     if (rc) return rc;
     K3_CUDA_TRY(cudaMemcpyAsync(out_host, ws.stage_out, xb, cudaMemcpyDeviceToHost, st));
     if (idx_host) K3_CUDA_TRY(cudaMemcpyAsync(idx_host, ws.stage_idx, kb, cudaMemcpyDeviceToHost, st));

@@ -92,6 +92,7 @@ struct k3moe_handle {
     const uint8_t **d_eptr[6] = {};            // device tables [E] for w1p,w1s,w3p,w3s,w2p,w2s
     const uint8_t **d_shtab = nullptr;         // device table [6]: shared ws1p,ws1s,ws3p,ws3s,ws2p,ws2s
     void *d_tmaps = nullptr;                   // tensor-path TMA descriptors (CUtensorMap[])
+    uint8_t *d_rowmax = nullptr;               // tensor-path per-row max exponent bytes
     size_t tmap_count = 0;
     k3_prof *prof = nullptr;                   // stage timing, when enabled
 };

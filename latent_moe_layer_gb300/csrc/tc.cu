@@ -1,16 +1,341 @@
-// Tensor-core path (tcgen05 + TMA).  Filled in by the grouped expert GEMMs.
-#include "tc.h"
+// Tensor-core path: TMA descriptors, load-time row maxima, activation prep and
+// the forward orchestration around the tcgen05 grouped expert GEMMs.
+#include <string.h>
+#include <vector>
 
-size_t k3_tc_tmap_count(const k3moe_config &c) { (void)c; return 0; }
+#include "tc.h"
+#include "tc_expert.cuh"
+
+using namespace k3;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// Packed MXFP4 matrix [rows, cols/2] bytes: box 32 bytes x 128 rows, 32-byte swizzle.
+bool encode_packed(CUtensorMap *m, const void *base, int rows, int cols)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(cols / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
+    cuuint32_t box[2] = {32, 128};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// f16 rows [rows, cols]: box 64 x bn, 128-byte swizzle.
+bool encode_act(CUtensorMap *m, const void *base, int rows, int cols, int bn)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)bn};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// rowmax[row] = max scale byte of the row; grid over (rows, groups).
+__global__ void rowmax_kernel(const uint8_t *const *tab, int groups, int rows, int kblk, uint8_t *out)
+{
+    const int g = blockIdx.y;
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= groups || r >= rows) return;
+    const uint8_t *p = tab[g] + (size_t)r * kblk;
+    uint32_t m = 0;
+    for (int i = 0; i < kblk; i += 16) {
+        uint4 v = *reinterpret_cast<const uint4 *>(p + i);
+        m = max(m, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+    }
+    m = max(max(m & 0xFF, (m >> 8) & 0xFF), max((m >> 16) & 0xFF, m >> 24));
+    out[(size_t)g * rows + r] = (uint8_t)m;
+}
+
+// One CTA per token: amax of the BF16 row, power-of-two factor 2^k with
+// amax * 2^k in [2^14, 2^15), f16 copies of the scaled row to each permuted row
+// of the token (row_of[t*K + k]) or to row t (row_of == nullptr), and the
+// inverse factor 2^-k per written row.
+__global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__restrict__ src, int cols,
+                                                           const int32_t *__restrict__ row_of, int K,
+                                                           __half *__restrict__ dst,
+                                                           float *__restrict__ rscale)
+{
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint16_t *s = src + (size_t)t * cols;
+    float amax = 0.f;
+    for (int i = tid * 8; i < cols; i += 256 * 8) {
+        uint4 v = *reinterpret_cast<const uint4 *>(s + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
+        }
+    }
+    __shared__ float red[8];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    int k = 0;
+    if (amax > 0.f && amax <= 3.0e38f) {
+        int ex;
+        frexpf(amax, &ex);                 // amax = m 2^ex, m in [0.5, 1)
+        k = 15 - ex;                        // amax 2^k in [2^14, 2^15)
+        k = max(-126, min(126, k));
+    }
+    const float up = __uint_as_float((uint32_t)(k + 127) << 23);
+    const float down = __uint_as_float((uint32_t)(127 - k) << 23);
+    for (int kk = 0; kk < K; ++kk) {
+        const int row = row_of ? row_of[(size_t)t * K + kk] : t;
+        __half *d = dst + (size_t)row * cols;
+        for (int i = tid * 8; i < cols; i += 256 * 8) {
+            uint4 v = *reinterpret_cast<const uint4 *>(s + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint4 o;
+            uint32_t *op = &o.x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __half2 hh = __floats2half2_rn(__uint_as_float(w[q] << 16) * up,
+                                               __uint_as_float(w[q] & 0xffff0000u) * up);
+                op[q] = *reinterpret_cast<uint32_t *>(&hh);
+            }
+            *reinterpret_cast<uint4 *>(d + i) = o;
+        }
+        if (tid == 0) rscale[row] = down;
+    }
+}
+
+// Token tiles of a dense (all-token) GEMM: (0, row0, rows) with at most bn rows.
+__global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
+{
+    const int n = (T + bn - 1) / bn;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) tiles[i] = make_int4(0, i * bn, min(bn, T - i * bn), 0);
+    if (threadIdx.x == 0) *count = n;
+}
+
+template <int NMAT, int BN, int NS, int MODE>
+int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
+{
+    using SM = ExpertSmem<NMAT, BN, NS>;
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, MODE>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        attr = true;
+    }
+    const int grid = max(1, min(num_sms, max_tiles));
+    kern<<<grid, (8 + 4 * NMAT) * 32, SM::BYTES, st>>>(bmap, a);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+// Tile shape by the token count per expert: small N for decode batches.
+int pick_bn(int T, int K, int E) { return ((size_t)T * K <= (size_t)E * 24) ? 32 : 128; }
+
+}  // namespace
+
+bool k3_tc_available() { return encode_fn() != nullptr; }
+
+size_t k3_tc_tmap_count(const k3moe_config &c) { return (size_t)3 * c.n_experts + 3; }
+
+size_t k3_tc_rowmax_bytes(const k3moe_config &c)
+{
+    return (size_t)c.n_experts * (2 * c.inter + c.latent) + (size_t)2 * c.shared_inter +
+           (c.shared_inter ? c.hidden : 0) + 64;
+}
 
 int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStream_t st)
 {
-    (void)h; (void)tabs; (void)st;
+    const k3moe_config &c = h->cfg;
+    const int E = c.n_experts, L = c.latent, I = c.inter, H = c.hidden, S = c.shared_inter;
+    if (!encode_fn()) return K3MOE_OK;          // tensor path unavailable; generic path serves
+    std::vector<CUtensorMap> maps(k3_tc_tmap_count(c));
+    memset(maps.data(), 0, maps.size() * sizeof(CUtensorMap));
+    for (int e = 0; e < E; ++e) {
+        if (!encode_packed(&maps[3 * e + 0], tabs[0][e], I, L)) return K3MOE_ERR_CUDA;
+        if (!encode_packed(&maps[3 * e + 1], tabs[2][e], I, L)) return K3MOE_ERR_CUDA;
+        if (!encode_packed(&maps[3 * e + 2], tabs[4][e], L, I)) return K3MOE_ERR_CUDA;
+    }
+    if (S > 0) {
+        if (!encode_packed(&maps[3 * E + 0], h->shared[0], S, H)) return K3MOE_ERR_CUDA;
+        if (!encode_packed(&maps[3 * E + 1], h->shared[2], S, H)) return K3MOE_ERR_CUDA;
+        if (!encode_packed(&maps[3 * E + 2], h->shared[4], H, S)) return K3MOE_ERR_CUDA;
+    }
+    K3_CUDA_TRY(cudaMemcpyAsync(h->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap),
+                                cudaMemcpyHostToDevice, st));
+    // per-row maximum exponent: [w1 E*I][w3 E*I][w2 E*L][ws1 S][ws3 S][ws2 H]
+    uint8_t *rm = h->d_rowmax;
+    rowmax_kernel<<<dim3((I + 127) / 128, E), 128, 0, st>>>(h->d_eptr[1], E, I, L / 32, rm);
+    rowmax_kernel<<<dim3((I + 127) / 128, E), 128, 0, st>>>(h->d_eptr[3], E, I, L / 32, rm + (size_t)E * I);
+    rowmax_kernel<<<dim3((L + 127) / 128, E), 128, 0, st>>>(h->d_eptr[5], E, L, I / 32, rm + (size_t)2 * E * I);
+    if (S > 0) {
+        uint8_t *rs = rm + (size_t)E * (2 * I + L);
+        rowmax_kernel<<<dim3((S + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 1), 1, S, H / 32, rs);
+        rowmax_kernel<<<dim3((S + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 3), 1, S, H / 32, rs + S);
+        rowmax_kernel<<<dim3((H + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 5), 1, H, S / 32, rs + 2 * S);
+    }
+    K3_CUDA_TRY(cudaGetLastError());
     return K3MOE_OK;
+}
+
+static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUtensorMap &b2,
+                       ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
+                       cudaStream_t st, int stage1, int stage2, bool f32_add)
+{
+    int rc;
+    {
+        k3_stage sg(h, stage1, st);
+        rc = bn == 32 ? launch_expert<2, 32, 8, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st)
+                      : launch_expert<2, 128, 4, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st);
+        if (rc) return rc;
+    }
+    {
+        k3_stage sg(h, stage2, st);
+        if (f32_add)
+            rc = bn == 32 ? launch_expert<1, 32, 8, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st)
+                          : launch_expert<1, 128, 4, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st);
+        else
+            rc = bn == 32 ? launch_expert<1, 32, 8, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st)
+                          : launch_expert<1, 128, 4, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st);
+    }
+    return rc;
 }
 
 int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws &ws, cudaStream_t st)
 {
-    (void)h; (void)x; (void)T; (void)out; (void)ws; (void)st;
-    return K3MOE_ERR_UNSUPPORTED;
+    const k3moe_config &c = h->cfg;
+    const int H = c.hidden, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter, S = c.shared_inter;
+    const int R = T * K;
+    const int bn = pick_bn(T, K, E);
+    int rc;
+    {
+        k3_stage sg(h, K3MOE_STAGE_ROUTER, st);
+        if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_router, c.router_dtype == K3MOE_ROUTER_BF16, E,
+                                      ws.logits, nullptr, 0, st)))
+            return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_DOWN, st);
+        if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_down, 1, L, nullptr, ws.h, 0, st))) return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_TOPK, st);
+        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
+        if ((rc = k3_launch_permute(h, ws, T, bn, st))) return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_PREP, st);
+        prep_f16_rows_kernel<<<T, 256, 0, st>>>(ws.h, L, ws.row_of, K, (__half *)ws.hperm, ws.hscale);
+        k3_note_launch();
+        K3_CUDA_TRY(cudaGetLastError());
+    }
+    const int max_ntiles = (R + bn - 1) / bn + (E < R ? E : R);
+    CUtensorMap bm1, bm2;
+    if (!encode_act(&bm1, ws.hperm, R, L, bn) || !encode_act(&bm2, ws.act, R, I, bn)) return K3MOE_ERR_CUDA;
+    const uint8_t *rm = h->d_rowmax;
+    ExpertGemmArgs a1 = {};
+    a1.amaps = (const CUtensorMap *)h->d_tmaps;
+    a1.amap_stride = 3;
+    a1.amap_off[0] = 0;
+    a1.amap_off[1] = 1;
+    a1.scales[0] = h->d_eptr[1];
+    a1.scales[1] = h->d_eptr[3];
+    a1.rowmax[0] = rm;
+    a1.rowmax[1] = rm + (size_t)E * I;
+    a1.rows = I;
+    a1.K = L;
+    a1.tiles = (const int4 *)ws.tiles;
+    a1.n_tiles = ws.meta + 1;
+    a1.rscale = ws.hscale;
+    a1.out = ws.act;
+    a1.status = h->d_status;
+    a1.spin_limit = 0xFFFFFFFFu;
+    ExpertGemmArgs a2 = a1;
+    a2.amap_off[0] = a2.amap_off[1] = 2;
+    a2.scales[0] = a2.scales[1] = h->d_eptr[5];
+    a2.rowmax[0] = a2.rowmax[1] = rm + (size_t)2 * E * I;
+    a2.rows = L;
+    a2.K = I;
+    a2.rscale = nullptr;
+    a2.out = ws.y;
+    if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM), st,
+                          K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false)))
+        return rc;
+    {
+        k3_stage sg(h, K3MOE_STAGE_COMBINE, st);
+        if ((rc = k3_launch_combine_norm(ws.y, 1, ws.row_of, ws.wts, h->gamma, T, K, L, c.rms_eps, ws.nrm, st)))
+            return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_UP, st);
+        if ((rc = k3_launch_rows_gemm(ws.nrm, 1, T, L, h->w_up, 1, H, ws.o32, nullptr, 0, st))) return rc;
+    }
+    if (S > 0) {
+        const int sbn = T <= 64 ? 32 : 128;
+        int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
+        {
+            k3_stage sg(h, K3MOE_STAGE_PREP, st);
+            prep_f16_rows_kernel<<<T, 256, 0, st>>>((const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
+                                                    ws.xscale);
+            k3_note_launch();
+            dense_tiles_kernel<<<1, 256, 0, st>>>(T, sbn, stiles, ws.meta + 2);
+            k3_note_launch();
+            K3_CUDA_TRY(cudaGetLastError());
+        }
+        CUtensorMap sb1, sb2;
+        if (!encode_act(&sb1, ws.xs, T, H, sbn) || !encode_act(&sb2, ws.sact, T, S, sbn)) return K3MOE_ERR_CUDA;
+        const uint8_t *rs = rm + (size_t)E * (2 * I + L);
+        ExpertGemmArgs s1 = a1;
+        s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;
+        s1.amap_stride = 3;
+        s1.scales[0] = k3_shared_tab(h, 1);
+        s1.scales[1] = k3_shared_tab(h, 3);
+        s1.rowmax[0] = rs;
+        s1.rowmax[1] = rs + S;
+        s1.rows = S;
+        s1.K = H;
+        s1.tiles = stiles;
+        s1.n_tiles = ws.meta + 2;
+        s1.rscale = ws.xscale;
+        s1.out = ws.sact;
+        ExpertGemmArgs s2 = s1;
+        s2.amap_off[0] = s2.amap_off[1] = 2;
+        s2.scales[0] = s2.scales[1] = k3_shared_tab(h, 5);
+        s2.rowmax[0] = s2.rowmax[1] = rs + 2 * S;
+        s2.rows = H;
+        s2.K = S;
+        s2.rscale = nullptr;
+        s2.out = ws.o32;
+        const int nt = (T + sbn - 1) / sbn;
+        if ((rc = expert_pair(h, sbn, sb1, sb2, s1, s2, nt * (S / EX_BM), nt * (H / EX_BM), st,
+                              K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED, true)))
+            return rc;
+    }
+    k3_stage sg(h, K3MOE_STAGE_FINISH, st);
+    return k3_launch_finish(ws.o32, T * H, (uint16_t *)out, st);
 }

@@ -2,8 +2,12 @@
 #pragma once
 #include "k3moe_internal.h"
 
+// Whether the tensor path is compiled in and usable.
+bool k3_tc_available();
 // Number of TMA descriptors the tensor path keeps in the persistent buffer.
 size_t k3_tc_tmap_count(const k3moe_config &c);
+// Bytes of per-row maximum-exponent data kept in the persistent buffer.
+size_t k3_tc_rowmax_bytes(const k3moe_config &c);
 // Build the descriptors and per-row scale data after the weights are recorded.
 int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStream_t st);
 // Full forward on the tensor path.

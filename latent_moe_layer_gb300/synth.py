@@ -91,7 +91,10 @@ CONFIGS = {
 # A small shape whose packed/scale rows are 16-byte aligned (the tensor-core
 # path's requirement) and that spans several 128-row tiles with a ragged tail.
 SMALL_ALIGNED = LayerConfig("small_aligned_t40", seed=10, wseed=10, T=40, H=1024, L=512, E=24,
-                            K=4, I=640, exp_lo=118, exp_hi=122)
+                            K=4, I=512, exp_lo=118, exp_hi=122)
+# The same with shared experts (merged intermediate 512).
+SMALL_SHARED = LayerConfig("small_shared_t40", seed=11, wseed=11, T=40, H=1024, L=512, E=24, K=4,
+                           I=512, S=512, exp_lo=118, exp_hi=122)
 
 
 # ---------------------------------------------------------------- helpers
