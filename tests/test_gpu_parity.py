@@ -60,13 +60,25 @@ def test_tiny_ragged_token_counts(T):
     assert_parity(compare(cfg, g, ref))
 
 
-@pytest.mark.parametrize("path", [GEN])
-def test_small_aligned_parity(path):
-    cfg = synth.SMALL_ALIGNED
+@pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
+@pytest.mark.parametrize("name,T", [("SMALL_ALIGNED", 40), ("SMALL_ALIGNED", 7), ("SMALL_ALIGNED", 300),
+                                    ("SMALL_SHARED", 40), ("SMALL_SHARED", 150)])
+def test_small_aligned_parity(path, name, T):
+    cfg = getattr(synth, name).with_tokens(T)
     g = run_gpu(cfg, path)
     assert g["status"] == 0
+    assert g["path"] == path
     ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
     assert_parity(compare(cfg, g, ref))
+
+
+def test_tensor_and_generic_paths_agree():
+    cfg = synth.SMALL_SHARED.with_tokens(64)
+    a = run_gpu(cfg, GEN)
+    b = run_gpu(cfg, TEN)
+    assert np.array_equal(a["idx"], b["idx"])
+    err = np.abs(a["out"] - b["out"]).max() / np.sqrt((a["out"] ** 2).mean())
+    assert err < 2e-2
 
 
 def test_batch_invariance():
@@ -186,16 +198,20 @@ def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0):
     return g, m
 
 
-def test_k3_decode_t16():
-    _k3_case(1, 16, 16)
+@pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
+def test_k3_decode_t16(path):
+    g, _ = _k3_case(1, 16, 16, path=path)
+    assert g["path"] == path
 
 
 def test_k3_decode_t256():
     _k3_case(2, 256, 48)
 
 
-def test_k3_prefill_t8192():
-    _k3_case(3, 512, 24)
+@pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
+def test_k3_prefill_t8192(path):
+    g, _ = _k3_case(3, 512, 24, path=path)
+    assert g["path"] == path
 
 
 def test_k3_prefill_t32768_skew_shared():
