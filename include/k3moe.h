@@ -165,6 +165,35 @@ const char *k3moe_strerror(int code);
 /* Which path k3moe_forward will take for T tokens: K3MOE_PATH_GENERIC or K3MOE_PATH_TENSOR. */
 int k3moe_path_for(const k3moe_handle *h, int T);
 
+/* ------------------------------------------------------------ allocation-free routing
+ * No counterpart in the sources: an extra entry point for callers that cannot
+ * allocate device memory at all (for example plugin hosts that give an
+ * operator only its input and output buffers and forbid device allocation
+ * while it runs, since cudaMalloc may block and synchronise the device and a
+ * caching allocator may already own all free memory).
+ *
+ * Computes the router logits and the top-K selection of k3moe_forward (same
+ * kernels, same results in idx_out [T, K] int32 and w_out [T, K] fp32, device
+ * memory) for x [T, H] BF16 (device, 16-byte aligned), with the fp32 logits
+ * scratch held in a static device array of K3MOE_ROUTE_STATIC_MAX_LOGITS
+ * floats (1 MiB) inside the library instead of caller workspace.  That array
+ * exists on every GPU that loads the library until the process exits.
+ *   - T * n_experts above K3MOE_ROUTE_STATIC_MAX_LOGITS: K3MOE_ERR_WORKSPACE,
+ *     nothing is launched.
+ *   - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *   - The first call on a device resolves the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the previous call's logits;
+ *     each call overwrites the T * n_experts values it reads.  Calls whose
+ *     work overlaps on the GPU (other streams, other threads, other handles)
+ *     race on the array and must be serialised by the caller.
+ */
+#define K3MOE_ROUTE_STATIC_MAX_LOGITS (256 * 1024)
+
+int k3moe_route_static(k3moe_handle *h, const void *x, int T, int32_t *idx_out, float *w_out,
+                       cudaStream_t stream);
+
 /* ------------------------------------------------------------ profiling
  * Stage timing with CUDA events recorded on the launching stream around each
  * stage of k3moe_forward (a ring of 256 forwards), plus a count of kernel
