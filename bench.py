@@ -189,6 +189,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     ge.build()
     cfg = synth.CONFIGS[args.config]
+    if args.experts:
+        # reduced expert count: for profiler captures that must stay a few GB on the device
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "E": args.experts, "name": cfg.name + f"_E{args.experts}"})
     pk, pk_src = peaks()
 
     dw = k3moe.DeviceWeights(cfg)
@@ -365,6 +368,7 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
+    ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling aid)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -1,0 +1,29 @@
+// Decode-batch streaming MXFP4 expert GEMV (gemv_expert.cu): arguments and launcher.
+#pragma once
+#include <cudaTypedefs.h>
+
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+enum GemvOut { GV_GLU_F16 = 0, GV_BF16 = 1, GV_F32_ADD = 2 };
+
+struct GemvArgs {
+    const CUtensorMap *amaps;          // global: packed map of group g, matrix m at amaps[g * amap_stride + amap_off[m]]
+    int amap_stride;
+    int amap_off[2];
+    const uint8_t *const *scales[2];   // [groups] of scale matrices [rows, K/32]
+    const uint8_t *rowmax[2];          // [groups * rows] per-row max exponent byte
+    int rows, K;                       // rows: multiple of 128; K: multiple of 512
+    const int4 *tiles;                 // (group, first B row, B rows <= 16) per token tile
+    const int *n_tiles;                // device count of tiles
+    const float *rscale;               // [R] per-row factor applied to the GLU inputs, or nullptr
+    void *out;                         // GLU: f16 [R, rows]; BF16: [R, rows]; F32_ADD: fp32 [R, rows]
+    int *status;
+};
+
+}  // namespace k3
+
+// bmap: f16 activation rows [R, K], box 64 x 16, 128-byte swizzle.
+int k3_launch_gemv_expert(int glu, int mode, const CUtensorMap &bmap, const k3::GemvArgs &args, int max_items,
+                          int num_sms, cudaStream_t st);

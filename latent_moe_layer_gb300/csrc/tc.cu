@@ -5,6 +5,7 @@
 
 #include "tc.h"
 #include "tc_expert.cuh"
+#include "gemv_expert.h"
 
 using namespace k3;
 
@@ -24,17 +25,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Packed MXFP4 matrix [rows, cols/2] bytes: box 32 bytes x 128 rows, 32-byte swizzle.
+// Packed MXFP4 matrix [rows, cols/2] bytes: box 128 bytes x 128 rows, 128-byte swizzle.
 bool encode_packed(CUtensorMap *m, const void *base, int rows, int cols)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(cols / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
-    cuuint32_t box[2] = {32, 128};
+    cuuint32_t box[2] = {128, 128};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -134,11 +135,12 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
     if (threadIdx.x == 0) *count = n;
 }
 
-template <int NMAT, int BN, int NS, int MODE>
+template <int NMAT, int BN, int NS, int NB, int NA, int MODE>
 int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
-    using SM = ExpertSmem<NMAT, BN, NS>;
-    auto kern = expert_gemm_kernel<NMAT, BN, NS, MODE>;
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
+    static_assert(SM::BYTES <= 227 * 1024, "shared memory");
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, MODE>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
@@ -200,6 +202,9 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
     return K3MOE_OK;
 }
 
+// Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA).
+//   decode (N <= 32):  gate/up 3/4/2 = 176 KB smem, down 4/4/4 = 144 KB
+//   prefill (N <= 128): gate/up 2/3/2 = 176 KB, down 3/4/3 = 160 KB
 static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUtensorMap &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool f32_add)
@@ -207,18 +212,18 @@ static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUt
     int rc;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32 ? launch_expert<2, 32, 8, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st)
-                      : launch_expert<2, 128, 4, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st);
+        rc = bn == 32 ? launch_expert<2, 32, 3, 4, 2, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st)
+                      : launch_expert<2, 128, 2, 3, 2, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st);
         if (rc) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
         if (f32_add)
-            rc = bn == 32 ? launch_expert<1, 32, 8, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st)
-                          : launch_expert<1, 128, 4, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st);
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st)
+                          : launch_expert<1, 128, 3, 4, 3, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st);
         else
-            rc = bn == 32 ? launch_expert<1, 32, 8, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st)
-                          : launch_expert<1, 128, 4, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st);
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st)
+                          : launch_expert<1, 128, 3, 4, 3, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st);
     }
     return rc;
 }
@@ -244,9 +249,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         k3_stage sg(h, K3MOE_STAGE_TOPK, st);
         if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
     }
-    {
+    {   // token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
         k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
-        if ((rc = k3_launch_permute(h, ws, T, bn, st))) return rc;
+        if ((rc = k3_launch_permute(h, ws, T, bn == 32 ? 16 : bn, st))) return rc;
     }
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
@@ -254,7 +259,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
-    const int max_ntiles = (R + bn - 1) / bn + (E < R ? E : R);
+    const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
     CUtensorMap bm1, bm2;
     if (!encode_act(&bm1, ws.hperm, R, L, bn) || !encode_act(&bm2, ws.act, R, I, bn)) return K3MOE_ERR_CUDA;
     const uint8_t *rm = h->d_rowmax;
@@ -283,9 +288,50 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a2.K = I;
     a2.rscale = nullptr;
     a2.out = ws.y;
-    if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM), st,
-                          K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false)))
+    if (bn == 32) {
+        // few tokens per expert: streaming GEMV, FP4 decoded in registers
+        GemvArgs g1 = {};
+        g1.amaps = (const CUtensorMap *)h->d_tmaps;
+        g1.amap_stride = 3;
+        g1.amap_off[0] = 0;
+        g1.amap_off[1] = 1;
+        g1.scales[0] = h->d_eptr[1];
+        g1.scales[1] = h->d_eptr[3];
+        g1.rowmax[0] = rm;
+        g1.rowmax[1] = rm + (size_t)E * I;
+        g1.rows = I;
+        g1.K = L;
+        g1.tiles = (const int4 *)ws.tiles;
+        g1.n_tiles = ws.meta + 1;
+        g1.rscale = ws.hscale;
+        g1.out = ws.act;
+        g1.status = h->d_status;
+        GemvArgs g2 = g1;
+        g2.amap_off[0] = g2.amap_off[1] = 2;
+        g2.scales[0] = g2.scales[1] = h->d_eptr[5];
+        g2.rowmax[0] = g2.rowmax[1] = rm + (size_t)2 * E * I;
+        g2.rows = L;
+        g2.K = I;
+        g2.rscale = nullptr;
+        g2.out = ws.y;
+        {
+            k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
+            CUtensorMap gb1;
+            if (!encode_act(&gb1, ws.hperm, R, L, 16)) return K3MOE_ERR_CUDA;
+            if ((rc = k3_launch_gemv_expert(1, GV_GLU_F16, gb1, g1, max_ntiles * (I / 128), h->num_sms, st)))
+                return rc;
+        }
+        {
+            k3_stage sg(h, K3MOE_STAGE_EXPERT_DOWN, st);
+            CUtensorMap gb2;
+            if (!encode_act(&gb2, ws.act, R, I, 16)) return K3MOE_ERR_CUDA;
+            if ((rc = k3_launch_gemv_expert(0, GV_BF16, gb2, g2, max_ntiles * (L / 128), h->num_sms, st)))
+                return rc;
+        }
+    } else if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM),
+                                 st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false))) {
         return rc;
+    }
     {
         k3_stage sg(h, K3MOE_STAGE_COMBINE, st);
         if ((rc = k3_launch_combine_norm(ws.y, 1, ws.row_of, ws.wts, h->gamma, T, K, L, c.rms_eps, ws.nrm, st)))

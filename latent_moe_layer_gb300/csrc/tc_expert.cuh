@@ -10,9 +10,13 @@
 // E2M1 x 2^(e - emax_m) in f16 -- exact for e >= emax_m - 23 -- and the factor
 // 2^(emax_m - 127) is applied to the fp32 accumulator in the epilogue.
 //
+// A packed stage feeds four 64-K MMA sub-steps; activation tiles have their
+// own ring so packed prefetch never waits on them.
+//
 // Roles (one CTA per SM, persistent over the tile list):
-//   warp 0            TMA producer: packed FP4 tiles (per-expert tensor maps,
-//                     32-byte swizzle) and activation rows (128-byte swizzle)
+//   warp 0            TMA producer of the packed FP4 tiles: 128 rows x 128 bytes
+//                     (256 K values) per stage, per-expert tensor maps, 128-byte swizzle
+//   warp 2            TMA producer of the f16 activation sub-tiles (64 K x N rows)
 //   warp 1            TMEM allocator and the single MMA-issuing thread
 //   warps 4..4+4*NMAT dequant: one thread per weight row, FP4 -> f16 into the
 //                     128-byte-swizzled K-major layout the MMA reads
@@ -46,19 +50,20 @@ struct ExpertGemmArgs {
 };
 
 constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
-constexpr int EX_BK = 64;            // K per stage (one 128-byte f16 row)
+constexpr int EX_KP = 256;           // K per packed stage (128-byte FP4 rows)
+constexpr int EX_KS = 64;            // K per MMA sub-step (one 128-byte f16 row)
+constexpr int EX_NSUB = EX_KP / EX_KS;
 
-template <int NMAT, int BN, int NS>
+template <int NMAT, int BN, int NS, int NB, int NA>
 struct ExpertSmem {
-    static constexpr int NA = 4 / NMAT;                     // f16 A slots (each NMAT tiles)
-    static constexpr int PK_BYTES = EX_BM * EX_BK / 2;      // 4096 packed bytes per matrix
-    static constexpr int B_BYTES = BN * EX_BK * 2;          // activation tile
-    static constexpr int A_BYTES = EX_BM * EX_BK * 2;       // 16384 f16 tile
+    static constexpr int PK_BYTES = EX_BM * EX_KP / 2;      // 16384 packed bytes per matrix
+    static constexpr int B_BYTES = BN * EX_KS * 2;          // activation sub-tile
+    static constexpr int A_BYTES = EX_BM * EX_KS * 2;       // 16384 f16 tile
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + NA * NMAT * A_BYTES;
-    static constexpr int OFF_PK = OFF_B + NS * B_BYTES;
+    static constexpr int OFF_PK = OFF_B + NB * B_BYTES;
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
-    static constexpr int N_BAR = 2 * NS + 2 * NA + 4 + 1;
+    static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1;
     static constexpr int BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + tmem holder/flag + align slack
 };
 
@@ -86,12 +91,21 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatil
     return false;
 }
 
-template <int NMAT, int BN, int NS, int MODE>
+// Drain: wait (wall-clock bounded) for the last min(n, ring) uses of a TMA ring.
+__device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int ring)
+{
+    const uint32_t n = issued < (uint32_t)ring ? issued : (uint32_t)ring;
+    for (uint32_t q = 0; q < n; ++q) {
+        const uint32_t i2 = issued - 1 - q;
+        mbar_wait(smem_u32(full + i2 % ring), (i2 / ring) & 1, 0xFFFFFFFFu);
+    }
+}
+
+template <int NMAT, int BN, int NS, int NB, int NA, int MODE>
 __global__ void __launch_bounds__((8 + 4 * NMAT) * 32, 1)
 expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArgs args)
 {
-    using SM = ExpertSmem<NMAT, BN, NS>;
-    constexpr int NA = SM::NA;
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     constexpr int EPI_WARP0 = 4 + 4 * NMAT;
     constexpr uint32_t TMEM_COLS = (2 * NMAT * BN <= 32) ? 32 : (2 * NMAT * BN <= 64) ? 64
                                  : (2 * NMAT * BN <= 128) ? 128 : (2 * NMAT * BN <= 256) ? 256 : 512;
@@ -100,21 +114,27 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + SM::OFF_BAR);
-    uint64_t *full = bars, *empty = bars + NS, *afull = bars + 2 * NS, *aempty = bars + 2 * NS + NA;
-    uint64_t *tfull = bars + 2 * NS + 2 * NA, *tempty = tfull + 2, *drain = tempty + 2;
+    uint64_t *pfull = bars, *pempty = pfull + NS;
+    uint64_t *bfull = pempty + NS, *bempty = bfull + NB;
+    uint64_t *afull = bempty + NB, *aempty = afull + NA;
+    uint64_t *tfull = aempty + NA, *tempty = tfull + 2, *drain = tempty + 2;
     uint32_t *tmem_holder = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int K = args.K, nk = K / EX_BK;
+    const int K = args.K, nkp = K / EX_KP;
     const int m_tiles = args.rows / EX_BM;
     const int total = __ldg(args.n_tiles) * m_tiles;
     const uint32_t lim = args.spin_limit;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(empty + i), 4 * NMAT + 1);
+            mbar_init(smem_u32(pfull + i), 1);
+            mbar_init(smem_u32(pempty + i), 4 * NMAT);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(smem_u32(bfull + i), 1);
+            mbar_init(smem_u32(bempty + i), 1);
         }
         for (int i = 0; i < NA; ++i) {
             mbar_init(smem_u32(afull + i), 4 * NMAT);
@@ -138,42 +158,63 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA: packed FP4 tiles
         if (lane == 0) {
-            prefetch_tmap(&bmap);
-            const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-            uint32_t it = 0;
+            const uint64_t pol_w = policy_evict_first();
+            uint32_t pit = 0;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
                 const int4 tile = __ldg(args.tiles + t / m_tiles);
-                const int g = tile.x, row0 = tile.y, m0 = (t % m_tiles) * EX_BM;
+                const int g = tile.x, m0 = (t % m_tiles) * EX_BM;
                 const CUtensorMap *am0 = args.amaps + (size_t)g * args.amap_stride + args.amap_off[0];
                 const CUtensorMap *am1 = args.amaps + (size_t)g * args.amap_stride + args.amap_off[NMAT - 1];
-                for (int s = 0; s < nk; ++s, ++it) {
-                    const int slot = it % NS;
-                    if (!role_wait(smem_u32(empty + slot), ((it / NS) & 1) ^ 1, abort_flag, lim,
-                                   args.status, 1))
+                bool ok = true;
+                for (int s = 0; s < nkp; ++s, ++pit) {
+                    const int slot = pit % NS;
+                    if (!role_wait(smem_u32(pempty + slot), ((pit / NS) & 1) ^ 1, abort_flag, lim,
+                                   args.status, 1)) {
+                        ok = false;
                         break;
-                    const uint32_t fb = smem_u32(full + slot);
-                    mbar_expect_tx(fb, NMAT * SM::PK_BYTES + SM::B_BYTES);
+                    }
+                    const uint32_t fb = smem_u32(pfull + slot);
+                    mbar_expect_tx(fb, NMAT * SM::PK_BYTES);
                     uint8_t *pk = smem + SM::OFF_PK + slot * NMAT * SM::PK_BYTES;
-                    tma_load_2d_hint(smem_u32(pk), am0, fb, s * (EX_BK / 2), m0, pol_w);
+                    tma_load_2d_hint(smem_u32(pk), am0, fb, s * (EX_KP / 2), m0, pol_w);
                     if (NMAT == 2)
-                        tma_load_2d_hint(smem_u32(pk + SM::PK_BYTES), am1, fb, s * (EX_BK / 2), m0, pol_w);
-                    tma_load_2d_hint(smem_u32(smem + SM::OFF_B + slot * SM::B_BYTES), &bmap, fb,
-                                     s * EX_BK, row0, pol_b);
+                        tma_load_2d_hint(smem_u32(pk + SM::PK_BYTES), am1, fb, s * (EX_KP / 2), m0, pol_w);
                 }
+                if (!ok) break;
             }
-            // drain: every issued stage must have landed before the CTA exits
-            const uint32_t n = it < (uint32_t)NS ? it : (uint32_t)NS;
-            for (uint32_t q = 0; q < n; ++q) {
-                const uint32_t i2 = it - 1 - q;
-                mbar_wait(smem_u32(full + i2 % NS), (i2 / NS) & 1, 0xFFFFFFFFu);
+            drain_ring(pfull, pit, NS);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ TMA: activation sub-tiles
+        if (lane == 0) {
+            prefetch_tmap(&bmap);
+            const uint64_t pol_b = policy_evict_last();
+            uint32_t bit = 0;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                const int row0 = __ldg(args.tiles + t / m_tiles).y;
+                bool ok = true;
+                for (int ks = 0; ks < K / EX_KS; ++ks, ++bit) {
+                    const int slot = bit % NB;
+                    if (!role_wait(smem_u32(bempty + slot), ((bit / NB) & 1) ^ 1, abort_flag, lim,
+                                   args.status, 8)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(bfull + slot);
+                    mbar_expect_tx(fb, SM::B_BYTES);
+                    tma_load_2d_hint(smem_u32(smem + SM::OFF_B + slot * SM::B_BYTES), &bmap, fb, ks * EX_KS,
+                                     row0, pol_b);
+                }
+                if (!ok) break;
             }
+            drain_ring(bfull, bit, NB);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, ait = 0, tc = 0;
+            uint32_t bit = 0, ait = 0, tc = 0;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
                 const int4 tile = __ldg(args.tiles + t / m_tiles);
                 const int nrows = tile.z;
@@ -185,27 +226,25 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                 tc_fence_after();
                 const uint32_t dcol = tmem + acc * NMAT * BN;
                 bool ok = true;
-                for (int s = 0; s < nk; ++s, ++it, ++ait) {
-                    const int slot = it % NS, aslot = ait % NA;
-                    if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, lim, args.status, 3) ||
+                for (int ks = 0; ks < K / EX_KS; ++ks, ++bit, ++ait) {
+                    const int bslot = bit % NB, aslot = ait % NA;
+                    if (!role_wait(smem_u32(bfull + bslot), (bit / NB) & 1, abort_flag, lim, args.status, 3) ||
                         !role_wait(smem_u32(afull + aslot), (ait / NA) & 1, abort_flag, lim, args.status, 4)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_addr = smem_u32(smem + SM::OFF_B + slot * SM::B_BYTES);
-                    const uint64_t bdesc = smem_desc_sw128(b_addr);
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + SM::OFF_B + bslot * SM::B_BYTES));
 #pragma unroll
                     for (int mt = 0; mt < NMAT; ++mt) {
-                        const uint32_t a_addr =
-                            smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES);
-                        const uint64_t adesc = smem_desc_sw128(a_addr);
+                        const uint64_t adesc =
+                            smem_desc_sw128(smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES));
 #pragma unroll
-                        for (int kk = 0; kk < EX_BK / 16; ++kk)
+                        for (int kk = 0; kk < EX_KS / 16; ++kk)
                             tc_mma_f16(dcol + mt * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                       (s > 0 || kk > 0) ? 1u : 0u);
+                                       (ks > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(empty + slot));
+                    tc_commit(smem_u32(bempty + bslot));
                     tc_commit(smem_u32(aempty + aslot));
                 }
                 if (!ok) break;
@@ -221,69 +260,99 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
         const int mat = d / 4;
         const int r = (d % 4) * 32 + lane;                 // weight row within the tile
         const int kblk = K / 32;
-        uint32_t it = 0, ait = 0;
-        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        uint32_t pit = 0, ait = 0;
+        // 16 scale bytes cover two packed stages; the next group is read one
+        // group ahead, and the next tile's first group during the current
+        // tile's last group
+        int t = blockIdx.x;
+        const uint8_t *srow = nullptr;
+        int emax = 0, emax_next = 0;
+        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = sc_cur;
+        if (t < total) {
             const int4 tile = __ldg(args.tiles + t / m_tiles);
-            const int g = tile.x, m0 = (t % m_tiles) * EX_BM;
-            const int row = m0 + r;
-            const int emax = __ldg(args.rowmax[mat] + (size_t)g * args.rows + row);
-            const uint8_t *srow = args.scales[mat][g] + (size_t)row * kblk;
-            uint4 sc_cur = __ldg(reinterpret_cast<const uint4 *>(srow));
-            uint4 sc_next = make_uint4(0, 0, 0, 0);
+            const int row = (t % m_tiles) * EX_BM + r;
+            emax = __ldg(args.rowmax[mat] + (size_t)tile.x * args.rows + row);
+            srow = args.scales[mat][tile.x] + (size_t)row * kblk;
+            sc_cur = __ldg(reinterpret_cast<const uint4 *>(srow));
+        }
+        for (; t < total && !*abort_flag; t += gridDim.x) {
+            const int tn = t + gridDim.x;
+            const uint8_t *srow_next = nullptr;
+            if (tn < total) {
+                const int4 tile = __ldg(args.tiles + tn / m_tiles);
+                const int row = (tn % m_tiles) * EX_BM + r;
+                srow_next = args.scales[mat][tile.x] + (size_t)row * kblk;
+                emax_next = __ldg(args.rowmax[mat] + (size_t)tile.x * args.rows + row);
+            }
             bool ok = true;
-            for (int s = 0; s < nk; ++s, ++it, ++ait) {
-                if ((s & 7) == 0) {
+            for (int s = 0; s < nkp; ++s, ++pit) {
+                if ((s & 1) == 0) {
                     if (s > 0) sc_cur = sc_next;
-                    if (s + 8 < nk) sc_next = __ldg(reinterpret_cast<const uint4 *>(srow) + (s >> 3) + 1);
+                    if (s + 2 < nkp) sc_next = __ldg(reinterpret_cast<const uint4 *>(srow) + (s >> 1) + 1);
+                    else if (srow_next) sc_next = __ldg(reinterpret_cast<const uint4 *>(srow_next));
                 }
-                const int slot = it % NS, aslot = ait % NA;
-                if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, lim, args.status, 5)) {
+                const int slot = pit % NS;
+                if (!role_wait(smem_u32(pfull + slot), (pit / NS) & 1, abort_flag, lim, args.status, 5)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *pk = smem + SM::OFF_PK + (slot * NMAT + mat) * SM::PK_BYTES + r * 32;
-                const int sw = (r >> 2) & 1;                   // 32-byte swizzle of the TMA box
-                const uint4 lo = *reinterpret_cast<const uint4 *>(pk + 16 * (0 ^ sw));
-                const uint4 hi = *reinterpret_cast<const uint4 *>(pk + 16 * (1 ^ sw));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(empty + slot));
-                // the two E8M0 bytes of this stage
-                const uint32_t sw32 = (&sc_cur.x)[(s & 7) >> 1];
-                const int e0 = (sw32 >> (16 * (s & 1))) & 0xFF, e1 = (sw32 >> (16 * (s & 1) + 8)) & 0xFF;
-                const uint32_t f0 = f16_pow2_bits(e0 - emax), f1 = f16_pow2_bits(e1 - emax);
-                const __half2 s0 = __halves2half2(__ushort_as_half((unsigned short)f0), __ushort_as_half((unsigned short)f0));
-                const __half2 s1 = __halves2half2(__ushort_as_half((unsigned short)f1), __ushort_as_half((unsigned short)f1));
-                if (!role_wait(smem_u32(aempty + aslot), ((ait / NA) & 1) ^ 1, abort_flag, lim, args.status, 6)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *arow = smem + SM::OFF_A + (aslot * NMAT + mat) * SM::A_BYTES + r * 128;
-                const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                // the row's 128 packed bytes (128-byte swizzle of the TMA box)
+                const uint8_t *pk = smem + SM::OFF_PK + (slot * NMAT + mat) * SM::PK_BYTES + r * 128;
+                uint4 c[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t h0, h1, h2, h3;
-                    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-                        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-                        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-                        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-                        : "r"(words[j]));
-                    const __half2 sc = j < 4 ? s0 : s1;
-                    __half2 q0 = __hmul2(*reinterpret_cast<__half2 *>(&h0), sc);
-                    __half2 q1 = __hmul2(*reinterpret_cast<__half2 *>(&h1), sc);
-                    __half2 q2 = __hmul2(*reinterpret_cast<__half2 *>(&h2), sc);
-                    __half2 q3 = __hmul2(*reinterpret_cast<__half2 *>(&h3), sc);
-                    uint4 v;
-                    v.x = *reinterpret_cast<uint32_t *>(&q0);
-                    v.y = *reinterpret_cast<uint32_t *>(&q1);
-                    v.z = *reinterpret_cast<uint32_t *>(&q2);
-                    v.w = *reinterpret_cast<uint32_t *>(&q3);
-                    *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
-                }
-                fence_proxy_async_smem();
+                for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (j ^ (r & 7)));
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(afull + aslot));
+                if (lane == 0) mbar_arrive(smem_u32(pempty + slot));
+                const uint32_t sw_lo = (s & 1) ? sc_cur.z : sc_cur.x;
+                const uint32_t sw_hi = (s & 1) ? sc_cur.w : sc_cur.y;
+#pragma unroll
+                for (int q = 0; q < EX_NSUB; ++q, ++ait) {
+                    const uint32_t sw32 = q < 2 ? sw_lo : sw_hi;
+                    const int e0 = (sw32 >> (16 * (q & 1))) & 0xFF, e1 = (sw32 >> (16 * (q & 1) + 8)) & 0xFF;
+                    const uint32_t f0 = f16_pow2_bits(e0 - emax), f1 = f16_pow2_bits(e1 - emax);
+                    const __half2 s0 = __halves2half2(__ushort_as_half((unsigned short)f0),
+                                                      __ushort_as_half((unsigned short)f0));
+                    const __half2 s1 = __halves2half2(__ushort_as_half((unsigned short)f1),
+                                                      __ushort_as_half((unsigned short)f1));
+                    const int aslot = ait % NA;
+                    if (!role_wait(smem_u32(aempty + aslot), ((ait / NA) & 1) ^ 1, abort_flag, lim,
+                                   args.status, 6)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *arow = smem + SM::OFF_A + (aslot * NMAT + mat) * SM::A_BYTES + r * 128;
+                    const uint4 lo = c[2 * q], hi = c[2 * q + 1];
+                    const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t h0, h1, h2, h3;
+                        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+                            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+                            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+                            : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+                            : "r"(words[j]));
+                        const __half2 sc = j < 4 ? s0 : s1;
+                        __half2 q0 = __hmul2(*reinterpret_cast<__half2 *>(&h0), sc);
+                        __half2 q1 = __hmul2(*reinterpret_cast<__half2 *>(&h1), sc);
+                        __half2 q2 = __hmul2(*reinterpret_cast<__half2 *>(&h2), sc);
+                        __half2 q3 = __hmul2(*reinterpret_cast<__half2 *>(&h3), sc);
+                        uint4 v;
+                        v.x = *reinterpret_cast<uint32_t *>(&q0);
+                        v.y = *reinterpret_cast<uint32_t *>(&q1);
+                        v.z = *reinterpret_cast<uint32_t *>(&q2);
+                        v.w = *reinterpret_cast<uint32_t *>(&q3);
+                        *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(afull + aslot));
+                }
+                if (!ok) break;
             }
             if (!ok) break;
+            srow = srow_next;
+            emax = emax_next;
+            sc_cur = sc_next;
         }
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue

@@ -12,7 +12,7 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libk3moe.so")
+LIB_PATH = os.environ.get("K3MOE_LIB", os.path.join(_PKG, "libk3moe.so"))
 
 OK = 0
 ERR = {0: "OK", -1: "ARG", -2: "SHAPE", -3: "ALIGN", -4: "BAD_SCALE", -5: "ALIAS", -6: "WORKSPACE",
