@@ -65,6 +65,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
     size_t ntm = k3_tc_tmap_count(c);
     void *tm = cv.take<uint8_t>(ntm * 128 + 128);
     uint8_t *rmax = cv.take<uint8_t>(k3_tc_rowmax_bytes(c));
+    uint16_t *hilo = cv.take<uint16_t>(k3_tc_hilo_bytes(c) / 2 + 1);
     int *flag = cv.take<int>(1);
     (void)flag;
     if (h) {
@@ -74,6 +75,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
         h->d_tmaps = base ? (void *)align_up((uintptr_t)tm, 128) : nullptr;
         h->tmap_count = ntm;
         h->d_rowmax = rmax;
+        h->d_router_hilo = hilo;
     }
     return align_up(cv.off, 256);
 }
@@ -318,6 +320,11 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->hscale = cv.take<float>(R + 1);
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
     ws->o32 = cv.take<float>(Tn * c.hidden);
+    {   // split-K partials for the decode-size dense GEMMs: up to 8 splits
+        const size_t w = (size_t)(c.n_experts + c.latent > c.hidden ? c.n_experts + c.latent : c.hidden);
+        ws->part_floats = T <= 256 ? (size_t)8 * Tn * w : 1;
+        ws->part = cv.take<float>(ws->part_floats);
+    }
     ws->sact = cv.take<float>(c.shared_inter ? Tn * c.shared_inter : 1);
     ws->xs = cv.take<uint16_t>(c.shared_inter ? Tn * c.hidden : 1);
     ws->xscale = cv.take<float>(Tn);

@@ -1,0 +1,288 @@
+// Dense BF16 GEMMs of the layer on tcgen05: router logits, routed_expert_down_proj
+// and routed_expert_up_proj ("Kimi K3, as released": the latent MoE's two dense
+// projections around the expert block; the router reads the same x).
+//
+// out[t, n] = sum_k X[t, k] W[n, k]: MMA M = 128 token rows (TMA; rows beyond T
+// are zero-filled by the copy engine), N = BN weight rows (TMA), K in 64-wide
+// steps, fp32 accumulators in TMEM.  Up to two segments of N share a launch,
+// each with its own weight tensor map, K and output: the router (fp32 weights
+// held as BF16 hi + lo, contracted over K' = 2H against x read twice, which
+// keeps the logits fp32-accurate) and the down projection run together.
+// Split-K writes fp32 partials that k3_launch_dense_reduce sums in a fixed order.
+#include <cudaTypedefs.h>
+
+#include "dense_tc.h"
+#include "ptx.cuh"
+
+namespace k3 {
+
+constexpr int DN_BM = 128;
+constexpr int DN_BK = 64;
+
+template <int BN, int NS>
+struct DenseSmem {
+    static constexpr int A_BYTES = DN_BM * DN_BK * 2;   // 16 KB
+    static constexpr int B_BYTES = BN * DN_BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int OFF_BAR = NS * STAGE;
+    static constexpr int BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
+};
+
+__device__ __forceinline__ bool dn_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
+                                        int where)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitCapNs) break;
+    }
+    set_status(status, K3MOE_ERR_TIMEOUT, where);
+    *abort_flag = 1;
+    return false;
+}
+
+template <int BN, int NS>
+__global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                                                            const __grid_constant__ CUtensorMap bmap0,
+                                                            const __grid_constant__ CUtensorMap bmap1,
+                                                            const DenseArgs args)
+{
+    using SM = DenseSmem<BN, NS>;
+    constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + SM::OFF_BAR), *empty = full + NS, *done = empty + NS;
+    uint32_t *tmem_holder = (uint32_t *)(done + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile -> (segment, n tile, m tile, split)
+    int tid = blockIdx.x;
+    const int mt_n = (args.M + DN_BM - 1) / DN_BM;
+    int seg = 0;
+    const int per0 = args.seg[0].n_tiles * mt_n * args.seg[0].splits;
+    if (tid >= per0) {
+        seg = 1;
+        tid -= per0;
+    }
+    const DenseSeg &S = args.seg[seg];
+    const int split = tid % S.splits;
+    tid /= S.splits;
+    const int mt = tid % mt_n;
+    const int nt = tid / mt_n;
+    const int n0 = nt * BN, m0 = mt * DN_BM;
+    const int ks_per = S.K / DN_BK / S.splits;
+    const int k0 = split * ks_per;
+    const CUtensorMap *bm = seg == 0 ? &bmap0 : &bmap1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 1);
+        }
+        mbar_init(smem_u32(done), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        prefetch_tmap(&amap);
+        prefetch_tmap(bm);
+        const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+        int issued = 0;
+        for (int s = 0; s < ks_per; ++s, ++issued) {
+            const int slot = s % NS;
+            if (!dn_wait(smem_u32(empty + slot), ((s / NS) & 1) ^ 1, abort_flag, args.status, 21)) break;
+            const uint32_t fb = smem_u32(full + slot);
+            mbar_expect_tx(fb, SM::STAGE);
+            uint8_t *st = smem + slot * SM::STAGE;
+            const int k = (k0 + s) * DN_BK;
+            tma_load_2d_hint(smem_u32(st), &amap, fb, k % S.a_kmod, m0, pol_a);
+            tma_load_2d_hint(smem_u32(st + SM::A_BYTES), bm, fb, k, n0, pol_w);
+        }
+        const int n = issued < NS ? issued : NS;
+        for (int q = 0; q < n; ++q) {
+            const int i2 = issued - 1 - q;
+            mbar_wait(smem_u32(full + i2 % NS), (i2 / NS) & 1, 0xFFFFFFFFu);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc = idesc_f16(DN_BM, BN, 1);
+        for (int s = 0; s < ks_per; ++s) {
+            const int slot = s % NS;
+            if (!dn_wait(smem_u32(full + slot), (s / NS) & 1, abort_flag, args.status, 22)) break;
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + slot * SM::STAGE);
+            const uint64_t adesc = smem_desc_sw128(a_addr), bdesc = smem_desc_sw128(a_addr + SM::A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < DN_BK / 16; ++kk)
+                tc_mma_f16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(empty + slot));
+        }
+        tc_commit(smem_u32(done));
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                       // TMEM lanes 32q .. 32q + 31
+        const int m = m0 + 32 * q + lane;
+        const bool ok = dn_wait(smem_u32(done), 0, abort_flag, args.status, 23);
+        tc_fence_after();
+        if (ok) {
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
+            for (int c = 0; c < BN / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(tbase + c * 16, v);
+                tc_wait_ld();
+                const int n = n0 + 16 * c;
+                const int nv = S.n_out - n;                 // valid columns in this chunk
+                if (m < args.M && nv > 0) {
+                    if (S.mode == DN_OUT_F32) {
+                        float *o = reinterpret_cast<float *>(S.out) + ((size_t)split * args.M + m) * S.ldo + S.col0 + n;
+                        if (nv >= 16) {
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4 *>(o + j) = make_float4(
+                                    __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < nv) o[j] = __uint_as_float(v[j]);
+                        }
+                    } else {
+                        uint16_t *o = reinterpret_cast<uint16_t *>(S.out) + (size_t)m * S.ldo + S.col0 + n;
+                        if (nv >= 16) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                pk[j] = (uint32_t)f32_to_bf16(__uint_as_float(v[2 * j])) |
+                                        ((uint32_t)f32_to_bf16(__uint_as_float(v[2 * j + 1])) << 16);
+                            *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            *reinterpret_cast<uint4 *>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < nv) o[j] = f32_to_bf16(__uint_as_float(v[j]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Sum split-K partials [splits][M][ldp] (columns [c0, c0 + n)) in split order.
+__global__ void dense_reduce_kernel(const float *__restrict__ part, int splits, int M, int ldp, int c0, int n,
+                                   float *__restrict__ out32, uint16_t *__restrict__ out16, int ldo)
+{
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)M * n) return;
+    const int m = (int)(i / n), j = (int)(i % n);
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[((size_t)s * M + m) * ldp + c0 + j];
+    if (out32) out32[(size_t)m * ldo + j] = acc;
+    if (out16) out16[(size_t)m * ldo + j] = f32_to_bf16(acc);
+}
+
+// Router weights fp32 [E, H] -> [E, 2H] BF16: hi = bf16(w) in columns [0, H), lo = bf16(w - hi) in [H, 2H).
+__global__ void split_hilo_kernel(const float *__restrict__ w, int E, int H, uint16_t *__restrict__ out)
+{
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)E * H) return;
+    const size_t e = i / H, k = i % H;
+    const float v = w[i];
+    const uint16_t hi = f32_to_bf16(v);
+    const uint16_t lo = f32_to_bf16(v - bf16_to_f32(hi));
+    out[e * 2 * H + k] = hi;
+    out[e * 2 * H + H + k] = lo;
+}
+
+}  // namespace k3
+
+using namespace k3;
+
+bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, int box_rows)
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NS>
+static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const DenseArgs &args,
+                        cudaStream_t st)
+{
+    using SM = DenseSmem<BN, NS>;
+    static_assert(SM::BYTES <= 227 * 1024, "shared memory");
+    auto kern = dense_gemm_kernel<BN, NS>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        attr = true;
+    }
+    const int mt = (args.M + DN_BM - 1) / DN_BM;
+    int grid = 0;
+    for (int s = 0; s < args.nseg; ++s) grid += args.seg[s].n_tiles * mt * args.seg[s].splits;
+    if (grid == 0) return K3MOE_OK;
+    kern<<<grid, 192, SM::BYTES, st>>>(a, b0, b1, args);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                       const DenseArgs &args, cudaStream_t st)
+{
+    if (bn == 128) return launch_dense<128, 3>(a, b0, b1, args, st);   // 2 CTAs per SM (decode sizes)
+    if (bn == 256) return launch_dense<256, 4>(a, b0, b1, args, st);
+    return K3MOE_ERR_UNSUPPORTED;
+}
+
+int k3_launch_dense_reduce(const float *part, int splits, int M, int ldp, int c0, int n, float *out32,
+                           uint16_t *out16, int ldo, cudaStream_t st)
+{
+    const size_t total = (size_t)M * n;
+    if (total == 0) return K3MOE_OK;
+    dense_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(part, splits, M, ldp, c0, n, out32, out16,
+                                                                         ldo);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3_launch_split_hilo(const float *w, int E, int H, uint16_t *out, cudaStream_t st)
+{
+    const size_t total = (size_t)E * H;
+    split_hilo_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(w, E, H, out);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}

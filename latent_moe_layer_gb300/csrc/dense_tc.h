@@ -1,0 +1,40 @@
+// Dense BF16 GEMMs on tcgen05 (dense_tc.cu): arguments and launchers.
+#pragma once
+#include <cudaTypedefs.h>
+
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+enum DenseOut { DN_OUT_F32 = 0, DN_OUT_BF16 = 1 };
+
+// One N segment: weight rows [0, n_out) of its tensor map (n_tiles tiles of BN rows).
+struct DenseSeg {
+    int n_tiles;     // ceil(n_out / BN)
+    int n_out;       // valid weight rows
+    int splits;      // split-K factor ((K / 64) % splits == 0)
+    int K;           // reduction length (multiple of 64)
+    int a_kmod;      // X column = k % a_kmod (router hi/lo: H; otherwise K)
+    int mode;        // DN_OUT_F32: out[(split * M + m) * ldo + col0 + n]; DN_OUT_BF16: out[m * ldo + col0 + n]
+    void *out;
+    int ldo;
+    int col0;
+};
+
+struct DenseArgs {
+    DenseSeg seg[2];
+    int nseg;
+    int M;           // token rows
+    int *status;
+};
+
+}  // namespace k3
+
+// X rows [rows, cols] BF16 (or weights): box 64 x box_rows, 128-byte swizzle.
+bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
+int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                       const k3::DenseArgs &args, cudaStream_t st);
+// out = sum over splits of part[s][m][c0 + j], j < n (fp32 and/or BF16 outputs, row stride ldo).
+int k3_launch_dense_reduce(const float *part, int splits, int M, int ldp, int c0, int n, float *out32,
+                           uint16_t *out16, int ldo, cudaStream_t st);
+int k3_launch_split_hilo(const float *w, int E, int H, uint16_t *out, cudaStream_t st);

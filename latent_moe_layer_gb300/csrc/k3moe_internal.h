@@ -93,6 +93,7 @@ struct k3moe_handle {
     const uint8_t **d_shtab = nullptr;         // device table [6]: shared ws1p,ws1s,ws3p,ws3s,ws2p,ws2s
     void *d_tmaps = nullptr;                   // tensor-path TMA descriptors (CUtensorMap[])
     uint8_t *d_rowmax = nullptr;               // tensor-path per-row max exponent bytes
+    uint16_t *d_router_hilo = nullptr;         // tensor-path router weights as BF16 [E, 2H] (hi | lo)
     size_t tmap_count = 0;
     k3_prof *prof = nullptr;                   // stage timing, when enabled
 };
@@ -138,6 +139,8 @@ struct k3_ws {
     float *hscale;        // [T*K] per-row power-of-two factor of hperm
     uint16_t *nrm;        // [T, L] BF16 normalised latent
     float *o32;           // [T, H] fp32 up_proj (+ shared) accumulator
+    float *part;          // split-K partials of the dense tensor-core GEMMs (small T only)
+    size_t part_floats;
     void *sact;           // [T, S] shared-expert activation (fp32 generic / f16 tensor)
     void *xs;             // [T, H] f16 scaled copy of x for the shared GLU (tensor path)
     float *xscale;        // [T]

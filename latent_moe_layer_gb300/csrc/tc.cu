@@ -6,6 +6,7 @@
 #include "tc.h"
 #include "tc_expert.cuh"
 #include "gemv_expert.h"
+#include "dense_tc.h"
 
 using namespace k3;
 
@@ -162,6 +163,11 @@ bool k3_tc_available() { return encode_fn() != nullptr; }
 
 size_t k3_tc_tmap_count(const k3moe_config &c) { return (size_t)3 * c.n_experts + 3; }
 
+size_t k3_tc_hilo_bytes(const k3moe_config &c)
+{
+    return c.router_dtype == K3MOE_ROUTER_F32 ? (size_t)c.n_experts * 2 * c.hidden * 2 : 0;
+}
+
 size_t k3_tc_rowmax_bytes(const k3moe_config &c)
 {
     return (size_t)c.n_experts * (2 * c.inter + c.latent) + (size_t)2 * c.shared_inter +
@@ -198,8 +204,124 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
         rowmax_kernel<<<dim3((S + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 3), 1, S, H / 32, rs + S);
         rowmax_kernel<<<dim3((H + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 5), 1, H, S / 32, rs + 2 * S);
     }
+    if (c.router_dtype == K3MOE_ROUTER_F32) {
+        int rc = k3_launch_split_hilo((const float *)h->w_router, E, H, h->d_router_hilo, st);
+        if (rc) return rc;
+    }
     K3_CUDA_TRY(cudaGetLastError());
     return K3MOE_OK;
+}
+
+// Smallest split-K factor (<= 8, dividing the K steps) giving at least `target` CTAs.
+static int choose_splits(int ksteps, int tiles, int target)
+{
+    int best = 1;
+    for (int sp = 1; sp <= 8; ++sp) {
+        if (ksteps % sp) continue;
+        best = sp;
+        if (tiles * sp >= target) return sp;
+    }
+    return best;
+}
+
+// Decode-size token counts use BN = 128 tiles and split-K into fp32 partials
+// (two CTAs per SM); larger counts use BN = 256 tiles writing outputs directly.
+static bool dense_small(const k3_ws &ws, int T, size_t width)
+{
+    return T <= 256 && ws.part_floats >= (size_t)8 * T * width;
+}
+
+// Router logits (fp32) and the latent h (BF16) in one tcgen05 launch.
+static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws &ws, cudaStream_t st)
+{
+    const k3moe_config &c = h->cfg;
+    const int H = c.hidden, L = c.latent, E = c.n_experts;
+    const bool small = dense_small(ws, T, (size_t)E + L);
+    const int bn = small ? 128 : 256;
+    const bool hilo = c.router_dtype == K3MOE_ROUTER_F32;
+    CUtensorMap ax, br, bd;
+    if (!k3_encode_bf16_rows(&ax, x, T, H, 128) ||
+        !k3_encode_bf16_rows(&br, hilo ? (const void *)h->d_router_hilo : h->w_router, E, hilo ? 2 * H : H, bn) ||
+        !k3_encode_bf16_rows(&bd, h->w_down, L, H, bn))
+        return K3MOE_ERR_CUDA;
+    const int mt = (T + 127) / 128;
+    DenseArgs a = {};
+    a.nseg = 2;
+    a.M = T;
+    a.status = h->d_status;
+    DenseSeg &r = a.seg[0], &d = a.seg[1];
+    r.n_out = E;
+    r.n_tiles = (E + bn - 1) / bn;
+    r.K = hilo ? 2 * H : H;
+    r.a_kmod = H;
+    d.n_out = L;
+    d.n_tiles = (L + bn - 1) / bn;
+    d.K = H;
+    d.a_kmod = H;
+    if (small) {
+        // split the work so both segments stream about the same bytes per CTA
+        const int target = 2 * h->num_sms;
+        const double wr = (double)r.K * E, wd = (double)d.K * L;
+        r.splits = choose_splits(r.K / 64, r.n_tiles * mt, (int)(target * wr / (wr + wd)));
+        d.splits = choose_splits(d.K / 64, d.n_tiles * mt, (int)(target * wd / (wr + wd)));
+        r.mode = d.mode = DN_OUT_F32;
+        r.out = d.out = ws.part;
+        r.ldo = d.ldo = E + L;
+        r.col0 = 0;
+        d.col0 = E;
+    } else {
+        r.splits = d.splits = 1;
+        r.mode = DN_OUT_F32;
+        r.out = ws.logits;
+        r.ldo = E;
+        r.col0 = 0;
+        d.mode = DN_OUT_BF16;
+        d.out = ws.h;
+        d.ldo = L;
+        d.col0 = 0;
+    }
+    int rc;
+    {
+        k3_stage sg(h, K3MOE_STAGE_ROUTER, st);
+        if ((rc = k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, st))) return rc;
+    }
+    if (small) {
+        k3_stage sg(h, K3MOE_STAGE_DOWN, st);
+        if ((rc = k3_launch_dense_reduce(ws.part, r.splits, T, E + L, 0, E, ws.logits, nullptr, E, st))) return rc;
+        if ((rc = k3_launch_dense_reduce(ws.part, d.splits, T, E + L, E, L, nullptr, ws.h, L, st))) return rc;
+    }
+    return K3MOE_OK;
+}
+
+// o32 = nrm W_up^T (fp32) on tcgen05.
+static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, cudaStream_t st)
+{
+    const k3moe_config &c = h->cfg;
+    const int H = c.hidden, L = c.latent;
+    const bool small = dense_small(ws, T, (size_t)H);
+    const int bn = small ? 128 : 256;
+    CUtensorMap an, bu;
+    if (!k3_encode_bf16_rows(&an, ws.nrm, T, L, 128) || !k3_encode_bf16_rows(&bu, h->w_up, H, L, bn))
+        return K3MOE_ERR_CUDA;
+    const int mt = (T + 127) / 128;
+    DenseArgs a = {};
+    a.nseg = 1;
+    a.M = T;
+    a.status = h->d_status;
+    DenseSeg &u = a.seg[0];
+    u.n_out = H;
+    u.n_tiles = (H + bn - 1) / bn;
+    u.K = L;
+    u.a_kmod = L;
+    u.mode = DN_OUT_F32;
+    u.col0 = 0;
+    u.ldo = H;
+    u.splits = small ? choose_splits(L / 64, u.n_tiles * mt, 2 * h->num_sms) : 1;
+    u.out = small ? ws.part : ws.o32;
+    int rc = k3_launch_dense_tc(bn, an, bu, bu, a, st);
+    if (rc) return rc;
+    if (small) rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, ws.o32, nullptr, H, st);
+    return rc;
 }
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA).
@@ -235,16 +357,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     const int R = T * K;
     const int bn = pick_bn(T, K, E);
     int rc;
-    {
-        k3_stage sg(h, K3MOE_STAGE_ROUTER, st);
-        if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_router, c.router_dtype == K3MOE_ROUTER_BF16, E,
-                                      ws.logits, nullptr, 0, st)))
-            return rc;
-    }
-    {
-        k3_stage sg(h, K3MOE_STAGE_DOWN, st);
-        if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_down, 1, L, nullptr, ws.h, 0, st))) return rc;
-    }
+    if ((rc = dense_router_down(h, x, T, ws, st))) return rc;
     {
         k3_stage sg(h, K3MOE_STAGE_TOPK, st);
         if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
@@ -339,7 +452,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     {
         k3_stage sg(h, K3MOE_STAGE_UP, st);
-        if ((rc = k3_launch_rows_gemm(ws.nrm, 1, T, L, h->w_up, 1, H, ws.o32, nullptr, 0, st))) return rc;
+        if ((rc = dense_up(h, T, ws, st))) return rc;
     }
     if (S > 0) {
         const int sbn = T <= 64 ? 32 : 128;

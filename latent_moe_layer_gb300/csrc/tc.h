@@ -8,6 +8,8 @@ bool k3_tc_available();
 size_t k3_tc_tmap_count(const k3moe_config &c);
 // Bytes of per-row maximum-exponent data kept in the persistent buffer.
 size_t k3_tc_rowmax_bytes(const k3moe_config &c);
+// Bytes of the router's BF16 hi/lo copy (0 when the router is stored BF16).
+size_t k3_tc_hilo_bytes(const k3moe_config &c);
 // Build the descriptors and per-row scale data after the weights are recorded.
 int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStream_t st);
 // Full forward on the tensor path.
