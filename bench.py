@@ -29,7 +29,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight GB/s vs HBM peak; prefill TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-EXPERT_BYTES = None   # set per config
+# DRAM bytes (read + write) per touched expert per launch, from the ncu capture in
+# profiles/gemv_expert_decode_dram.md (decode GEMV, 128-expert case, scaled by
+# touched experts).  Valid only while those kernels are unchanged.
+NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.15e6, ("expert_down", "gemv"): 5.874e6}
 
 
 def peaks():
@@ -162,14 +165,20 @@ def dist_setup(n_gpus):
     return world, rank, local
 
 
-def reduce_max(v, world):
+def reduce_max(v, world, device="cuda"):
+    """Max of a per-rank scalar over all ranks (the job's wall time is the slowest replica)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(tokens_per_step, steps, max_total_ms, world):
+    """Tokens/s of the whole job: every replica processes its own batch each step."""
+    return world * tokens_per_step * steps / (max_total_ms / 1e3)
 
 
 def barrier(world):
@@ -242,7 +251,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {st}")
     total_ms = reduce_max(total_ms, world)
     ms_step = total_ms / args.steps
-    value = world * cfg.T * args.steps / (total_ms / 1e3)
+    value = whole_job_value(cfg.T, args.steps, total_ms, world)
 
     # roofline of the dominant stage
     work = stage_work(cfg, touched, path_tensor)
@@ -259,6 +268,10 @@ def run_ours(args):
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "traffic": None}
+    key = (dom, "gemv" if (path_tensor and cfg.T * cfg.K <= cfg.E * 24) else "other")
+    if key in NCU_TRAFFIC_PER_EXPERT:
+        roof["traffic"] = round(NCU_TRAFFIC_PER_EXPERT[key] * touched)
+        roof["traffic_source"] = "ncu dram bytes per touched expert x touched experts"
     roof.update({"kernel_stage": dom, "per_launch_ms": round(per_launch_ms, 4),
                  "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": pk_src})
 
@@ -280,7 +293,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ee), world)
-        e2e = {"value": round(world * cfg.T * args.steps / (e_ms / 1e3), 2), "unit": "tokens/s",
+        e2e = {"value": round(whole_job_value(cfg.T, args.steps, e_ms, world), 2), "unit": "tokens/s",
                "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2,
                "ms_per_step": round(e_ms / args.steps, 4)}
 

@@ -172,9 +172,12 @@ int k3moe_path_for(const k3moe_handle *h, int T);
  * while it runs, since cudaMalloc may block and synchronise the device and a
  * caching allocator may already own all free memory).
  *
- * Computes the router logits and the top-K selection of k3moe_forward (same
- * kernels, same results in idx_out [T, K] int32 and w_out [T, K] fp32, device
- * memory) for x [T, H] BF16 (device, 16-byte aligned), with the fp32 logits
+ * Computes the router logits and the top-K selection (idx_out [T, K] int32 and
+ * w_out [T, K] fp32, device memory, as k3moe_forward returns them) for
+ * x [T, H] BF16 (device, 16-byte aligned).  The logits come from the fp32
+ * CUDA-core GEMM of the generic path (k3moe_forward's tensor path computes them
+ * on the tensor cores from BF16 hi + lo weights; the two agree to ~1e-6) and
+ * the selection from the same top-K kernel.  The fp32 logits
  * scratch held in a static device array of K3MOE_ROUTE_STATIC_MAX_LOGITS
  * floats (1 MiB) inside the library instead of caller workspace.  That array
  * exists on every GPU that loads the library until the process exits.
