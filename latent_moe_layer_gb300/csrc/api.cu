@@ -321,7 +321,8 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
     ws->o32 = cv.take<float>(Tn * c.hidden);
     {   // split-K partials for the decode-size dense GEMMs: up to 8 splits
-        const size_t w = (size_t)(c.n_experts + c.latent > c.hidden ? c.n_experts + c.latent : c.hidden);
+        const size_t ep = (size_t)((c.n_experts + 15) & ~15);
+        const size_t w = ep + c.latent > (size_t)c.hidden ? ep + c.latent : (size_t)c.hidden;
         ws->part_floats = T <= 256 ? (size_t)8 * Tn * w : 1;
         ws->part = cv.take<float>(ws->part_floats);
     }

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
                 if (m < args.M && nv > 0) {
                     if (S.mode == DN_OUT_F32) {
                         float *o = reinterpret_cast<float *>(S.out) + ((size_t)split * args.M + m) * S.ldo + S.col0 + n;
-                        if (nv >= 16) {
+                        if (nv >= 16 && ((uintptr_t)o & 15) == 0) {
 #pragma unroll
                             for (int j = 0; j < 16; j += 4)
                                 *reinterpret_cast<float4 *>(o + j) = make_float4(
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
                         }
                     } else {
                         uint16_t *o = reinterpret_cast<uint16_t *>(S.out) + (size_t)m * S.ldo + S.col0 + n;
-                        if (nv >= 16) {
+                        if (nv >= 16 && ((uintptr_t)o & 15) == 0) {
                             uint32_t pk[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j)

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                         hb[nb][1] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c + 1) ^ (br & 7)));
                     }
                     if (ks == 3) {
+                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(empty + slot));
                     }

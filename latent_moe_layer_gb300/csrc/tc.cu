@@ -236,7 +236,8 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
 {
     const k3moe_config &c = h->cfg;
     const int H = c.hidden, L = c.latent, E = c.n_experts;
-    const bool small = dense_small(ws, T, (size_t)E + L);
+    const int Ep = (E + 15) & ~15;
+    const bool small = dense_small(ws, T, (size_t)Ep + L);
     const int bn = small ? 128 : 256;
     const bool hilo = c.router_dtype == K3MOE_ROUTER_F32;
     CUtensorMap ax, br, bd;
@@ -264,11 +265,12 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
         const double wr = (double)r.K * E, wd = (double)d.K * L;
         r.splits = choose_splits(r.K / 64, r.n_tiles * mt, (int)(target * wr / (wr + wd)));
         d.splits = choose_splits(d.K / 64, d.n_tiles * mt, (int)(target * wd / (wr + wd)));
+        // partial columns: router [0, Ep), down [Ep, Ep + L); Ep rounds E to 16 floats
         r.mode = d.mode = DN_OUT_F32;
         r.out = d.out = ws.part;
-        r.ldo = d.ldo = E + L;
+        r.ldo = d.ldo = Ep + L;
         r.col0 = 0;
-        d.col0 = E;
+        d.col0 = Ep;
     } else {
         r.splits = d.splits = 1;
         r.mode = DN_OUT_F32;
@@ -287,8 +289,8 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     }
     if (small) {
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
-        if ((rc = k3_launch_dense_reduce(ws.part, r.splits, T, E + L, 0, E, ws.logits, nullptr, E, st))) return rc;
-        if ((rc = k3_launch_dense_reduce(ws.part, d.splits, T, E + L, E, L, nullptr, ws.h, L, st))) return rc;
+        if ((rc = k3_launch_dense_reduce(ws.part, r.splits, T, Ep + L, 0, E, ws.logits, nullptr, E, st))) return rc;
+        if ((rc = k3_launch_dense_reduce(ws.part, d.splits, T, Ep + L, Ep, L, nullptr, ws.h, L, st))) return rc;
     }
     return K3MOE_OK;
 }

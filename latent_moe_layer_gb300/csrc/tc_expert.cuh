@@ -301,6 +301,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                 uint4 c[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (j ^ (r & 7)));
+                // the stage is refilled by TMA (async proxy): order these generic reads before it
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(pempty + slot));
                 const uint32_t sw_lo = (s & 1) ? sc_cur.z : sc_cur.x;
