@@ -280,6 +280,59 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(
     }
 }
 
+// Vectorised combine + RMSNorm for BF16 y: one thread per 8 latent elements (L / 8 threads).
+__global__ void __launch_bounds__(1024) combine_norm_v8_kernel(
+    const uint16_t *__restrict__ y, const int32_t *__restrict__ row_of, const float *__restrict__ wts,
+    const uint16_t *__restrict__ gamma, int K, int L, float eps, uint16_t *__restrict__ nrm)
+{
+    const int t = blockIdx.x, tid = threadIdx.x;
+    __shared__ float red[32];
+    __shared__ int rows[64];
+    __shared__ float ws_[64];
+    if (tid < K) {
+        rows[tid] = row_of[(size_t)t * K + tid];
+        ws_[tid] = wts[(size_t)t * K + tid];
+    }
+    __syncthreads();
+    const int i = tid * 8;
+    float z[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) z[q] = 0.f;
+    if (i < L) {
+        for (int k = 0; k < K; ++k) {      // fixed k order
+            const uint4 v = *reinterpret_cast<const uint4 *>(y + (size_t)rows[k] * L + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const float wk = ws_[k];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                z[2 * q] = fmaf(wk, __uint_as_float(w[q] << 16), z[2 * q]);
+                z[2 * q + 1] = fmaf(wk, __uint_as_float(w[q] & 0xffff0000u), z[2 * q + 1]);
+            }
+        }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ss = fmaf(z[q], z[q], ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    const int nw = (blockDim.x + 31) >> 5;
+    for (int w = 0; w < nw; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)L + eps);
+    if (i < L) {
+        const uint4 g = *reinterpret_cast<const uint4 *>(gamma + i);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            o[q] = (uint32_t)f32_to_bf16(z[2 * q] * inv * __uint_as_float(gw[q] << 16)) |
+                   ((uint32_t)f32_to_bf16(z[2 * q + 1] * inv * __uint_as_float(gw[q] & 0xffff0000u)) << 16);
+        *reinterpret_cast<uint4 *>(nrm + (size_t)t * L + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 __global__ void finish_kernel(const float *__restrict__ o32, size_t n, uint16_t *__restrict__ out)
 {
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -366,6 +419,12 @@ int k3_launch_combine_norm(const void *y, int y_bf16, const int32_t *row_of, con
 {
     if (T == 0) return K3MOE_OK;
     if (L > 256 * CN_MAXV || K > 64) return K3MOE_ERR_UNSUPPORTED;
+    if (y_bf16 && L % 8 == 0 && L / 8 <= 1024) {
+        const int threads = ((L / 8) + 31) / 32 * 32;
+        combine_norm_v8_kernel<<<T, threads, 0, st>>>((const uint16_t *)y, row_of, wts, gamma, K, L, eps, nrm);
+        k3_note_launch();
+        return K3_LAUNCH_OK();
+    }
     combine_norm_kernel<<<T, 256, 0, st>>>(y, y_bf16, row_of, wts, gamma, K, L, eps, nrm);
     k3_note_launch();
     return K3_LAUNCH_OK();

@@ -11,72 +11,93 @@
 
 namespace k3 {
 
-// One warp per token.  Lane l holds keys j = l + 32 i.  Each of the K rounds
-// takes the warp-wide maximum key, lower index first on equal keys; NaN keys
-// rank below every number.  Writes idx in selection order and the mixture
-// weights sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
+// One warp per token (8 tokens per CTA).  Lane l owns keys j = l + 32 i (a
+// column of a [MAXP][32] tile in shared memory) and keeps the best untaken key
+// of its column.  Each of the K rounds takes the warp-wide maximum of the lane
+// bests (equal keys: lower index), marks it taken, and the warp rescans only the
+// winning lane's column.  NaN keys rank below every number.  Writes idx in
+// selection order and the weights sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
 template <int MAXP>
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits,
                                                    const float *__restrict__ bias, int T, int E,
                                                    int K, float scaling, int32_t *__restrict__ idx,
                                                    float *__restrict__ wts)
 {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    __shared__ float skey[8][MAXP][32];
+    const int wl = threadIdx.x >> 5;
+    const int warp = blockIdx.x * 8 + wl;
     const int lane = threadIdx.x & 31;
     if (warp >= T) return;
     const float *lrow = logits + (size_t)warp * E;
-    float key[MAXP];
+    float (*col)[32] = skey[wl];
+    float bk = -INFINITY;
+    int bj = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < MAXP; ++i) {
-        int j = lane + 32 * i;
+        const int j = lane + 32 * i;
         float k = -INFINITY;
         if (j < E) {
-            float l = lrow[j];
-            if (bias) k = 1.0f / (1.0f + expf(-l)) + bias[j];
-            else k = l;
+            const float l = lrow[j];
+            k = bias ? 1.0f / (1.0f + expf(-l)) + bias[j] : l;
             if (k != k) k = -INFINITY;
-        }
-        key[i] = k;
-    }
-    uint32_t taken = 0;
-    int mine = -1;            // selection slot this lane writes (lane s writes slot s)
-    float ssum = 0.f;
-    int sel_j = 0;
-    for (int s = 0; s < K; ++s) {
-        float bk = -INFINITY;
-        int bj = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < MAXP; ++i) {
-            int j = lane + 32 * i;
-            bool free_ = !((taken >> i) & 1u) && j < E;
-            if (free_ && (key[i] > bk || (key[i] == bk && j < bj))) {
-                bk = key[i];
+            if (k > bk || bj == 0x7fffffff) {     // first valid key, then strictly larger
+                bk = k;
                 bj = j;
+            }
+        }
+        col[i][lane] = k;
+    }
+    __syncwarp();
+    uint32_t taken = 0;          // bit i: key lane + 32 i taken (owner lane's view)
+    int sel_j = 0;
+    float ssum = 0.f;
+    for (int s = 0; s < K; ++s) {
+        float wk = bk;
+        int wj = bj;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, wk, off);
+            const int oj = __shfl_xor_sync(0xffffffffu, wj, off);
+            if (ok > wk || (ok == wk && oj < wj)) {
+                wk = ok;
+                wj = oj;
+            }
+        }
+        const int owner = wj & 31;
+        if (lane == owner) taken |= 1u << (wj >> 5);
+        const uint32_t otaken = __shfl_sync(0xffffffffu, taken, owner);
+        // rescan the owner's column: lane i looks at key owner + 32 i
+        float ck = -INFINITY;
+        int cj = 0x7fffffff;
+        if (lane < MAXP) {
+            const int j = owner + 32 * lane;
+            if (j < E && !((otaken >> lane) & 1u)) {
+                ck = col[lane][owner];
+                cj = j;
             }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-            int oj = __shfl_xor_sync(0xffffffffu, bj, off);
-            if (ok > bk || (ok == bk && oj < bj)) {
-                bk = ok;
-                bj = oj;
+            const float ok = __shfl_xor_sync(0xffffffffu, ck, off);
+            const int oj = __shfl_xor_sync(0xffffffffu, cj, off);
+            if (ok > ck || (ok == ck && oj < cj)) {
+                ck = ok;
+                cj = oj;
             }
         }
-        if ((bj & 31) == lane) taken |= 1u << (bj >> 5);
-        float l = lrow[bj];
-        float sg = 1.0f / (1.0f + expf(-l));
-        ssum += sg;
-        if (lane == s) {
-            mine = s;
-            sel_j = bj;
+        if (lane == owner) {
+            bk = ck;
+            bj = cj;
         }
+        const float l = lrow[wj];
+        ssum += 1.0f / (1.0f + expf(-l));
+        if (lane == s) sel_j = wj;
     }
-    if (mine >= 0) {
-        float l = lrow[sel_j];
-        float sg = 1.0f / (1.0f + expf(-l));
-        idx[(size_t)warp * K + mine] = sel_j;
-        wts[(size_t)warp * K + mine] = sg / ssum * scaling;
+    if (lane < K) {
+        const float l = lrow[sel_j];
+        const float sg = 1.0f / (1.0f + expf(-l));
+        idx[(size_t)warp * K + lane] = sel_j;
+        wts[(size_t)warp * K + lane] = sg / ssum * scaling;
     }
 }
 

@@ -295,8 +295,9 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     return K3MOE_OK;
 }
 
-// o32 = nrm W_up^T (fp32) on tcgen05.
-static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, cudaStream_t st)
+// o32 = nrm W_up^T (fp32) on tcgen05; with out16 (no shared experts) the BF16
+// output is written directly and o32 is not touched.
+static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cudaStream_t st)
 {
     const k3moe_config &c = h->cfg;
     const int H = c.hidden, L = c.latent;
@@ -315,14 +316,15 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, cudaStream_t st)
     u.n_tiles = (H + bn - 1) / bn;
     u.K = L;
     u.a_kmod = L;
-    u.mode = DN_OUT_F32;
+    u.mode = (!small && out16) ? DN_OUT_BF16 : DN_OUT_F32;
     u.col0 = 0;
     u.ldo = H;
     u.splits = small ? choose_splits(L / 64, u.n_tiles * mt, 2 * h->num_sms) : 1;
-    u.out = small ? ws.part : ws.o32;
+    u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
     int rc = k3_launch_dense_tc(bn, an, bu, bu, a, st);
     if (rc) return rc;
-    if (small) rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, ws.o32, nullptr, H, st);
+    if (small)
+        rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, out16 ? nullptr : ws.o32, out16, H, st);
     return rc;
 }
 
@@ -454,8 +456,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     {
         k3_stage sg(h, K3MOE_STAGE_UP, st);
-        if ((rc = dense_up(h, T, ws, st))) return rc;
+        if ((rc = dense_up(h, T, ws, S > 0 ? nullptr : (uint16_t *)out, st))) return rc;
     }
+    if (S == 0) return K3MOE_OK;                 // the up-projection wrote the BF16 output
     if (S > 0) {
         const int sbn = T <= 64 ? 32 : 128;
         int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
