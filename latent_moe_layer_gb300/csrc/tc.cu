@@ -136,12 +136,12 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
     if (threadIdx.x == 0) *count = n;
 }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int MODE>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
 int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
-    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, MODE>;
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
@@ -155,7 +155,12 @@ int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tile
 }
 
 // Tile shape by the token count per expert: small N for decode batches.
-int pick_bn(int T, int K, int E) { return ((size_t)T * K <= (size_t)E * 24) ? 32 : 128; }
+int pick_bn(int T, int K, int E)
+{
+    const size_t R = (size_t)T * K;
+    if (R <= (size_t)E * 24) return 32;
+    return R >= (size_t)E * 512 ? 128 : 256;
+}
 
 }  // namespace
 
@@ -328,28 +333,37 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     return rc;
 }
 
-// Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA).
-//   decode (N <= 32):  gate/up 3/4/2 = 176 KB smem, down 4/4/4 = 144 KB
-//   prefill (N <= 128): gate/up 2/3/2 = 176 KB, down 3/4/3 = 160 KB
+// Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
+// accumulator sets NACC).  N <= 32: gate/up 3/4/2/2 (176 KB smem), down 4/4/4/2 (144 KB);
+// N <= 128: gate/up 2/3/2/2 (176 KB), down 3/4/3/2 (160 KB); N <= 256: gate/up 2/2/2/1 (192 KB; 512 TMEM columns),
+// down 3/3/3/2 (192 KB).  bn selects the tile shape: 32 (tensor path at decode sizes, shared experts),
+// 128 (many tokens per expert: double-buffered accumulators overlap the GLU
+// epilogue with the next tile) or 256 (fewer tokens per expert: one dequantised
+// weight tile serves up to 256 tokens).
 static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUtensorMap &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool f32_add)
 {
     int rc;
+    const int ns = h->num_sms;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32 ? launch_expert<2, 32, 3, 4, 2, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st)
-                      : launch_expert<2, 128, 2, 3, 2, OUT_GLU_F16>(b1, a1, max_tiles1, h->num_sms, st);
+        rc = bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
+             : bn == 128 ? launch_expert<2, 128, 2, 3, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
+                         : launch_expert<2, 256, 2, 2, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
+        // the activation tensor map's box is bn rows: the kernel's BN must equal bn
         if (f32_add)
-            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st)
-                          : launch_expert<1, 128, 3, 4, 3, OUT_F32_ADD>(b2, a2, max_tiles2, h->num_sms, st);
+            rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
+                 : bn == 128 ? launch_expert<1, 128, 3, 4, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
+                             : launch_expert<1, 256, 3, 3, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
         else
-            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st)
-                          : launch_expert<1, 128, 3, 4, 3, OUT_BF16>(b2, a2, max_tiles2, h->num_sms, st);
+            rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
+                 : bn == 128 ? launch_expert<1, 128, 3, 4, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
+                             : launch_expert<1, 256, 3, 3, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
 }
@@ -460,7 +474,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     if (S == 0) return K3MOE_OK;                 // the up-projection wrote the BF16 output
     if (S > 0) {
-        const int sbn = T <= 64 ? 32 : 128;
+        const int sbn = T <= 64 ? 32 : 256;
         int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
         {
             k3_stage sg(h, K3MOE_STAGE_PREP, st);

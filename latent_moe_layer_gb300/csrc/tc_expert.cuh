@@ -101,15 +101,16 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
     }
 }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int MODE>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
 __global__ void __launch_bounds__((8 + 4 * NMAT) * 32, 1)
 expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArgs args)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     constexpr int EPI_WARP0 = 4 + 4 * NMAT;
-    constexpr uint32_t TMEM_COLS = (2 * NMAT * BN <= 32) ? 32 : (2 * NMAT * BN <= 64) ? 64
-                                 : (2 * NMAT * BN <= 128) ? 128 : (2 * NMAT * BN <= 256) ? 256 : 512;
-    static_assert(2 * NMAT * BN <= 512, "TMEM columns");
+    constexpr int COLS = NACC * NMAT * BN;       // NACC accumulator sets (2: epilogue overlaps the next tile)
+    constexpr uint32_t TMEM_COLS = (COLS <= 32) ? 32 : (COLS <= 64) ? 64 : (COLS <= 128) ? 128
+                                 : (COLS <= 256) ? 256 : 512;
+    static_assert(COLS <= 512 && (NACC == 1 || NACC == 2), "TMEM columns");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -220,8 +221,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                 const int nrows = tile.z;
                 const int nmma = min(BN, max(16, (nrows + 15) & ~15));
                 const uint32_t idesc = idesc_f16(EX_BM, nmma, 0);
-                const int acc = tc & 1;
-                if (!role_wait(smem_u32(tempty + acc), ((tc >> 1) & 1) ^ 1, abort_flag, lim, args.status, 2))
+                const int acc = (int)(tc % NACC);
+                if (!role_wait(smem_u32(tempty + acc), ((tc / NACC) & 1) ^ 1, abort_flag, lim, args.status, 2))
                     break;
                 tc_fence_after();
                 const uint32_t dcol = tmem + acc * NMAT * BN;
@@ -365,10 +366,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
             const int4 tile = __ldg(args.tiles + t / m_tiles);
             const int g = tile.x, row0 = tile.y, nrows = tile.z;
             const int m0 = (t % m_tiles) * EX_BM, row = m0 + r;
-            const int acc = tc & 1;
+            const int acc = (int)(tc % NACC);
             const float fw0 = e8m0_to_f32(__ldg(args.rowmax[0] + (size_t)g * args.rows + row));
             const float fw1 = NMAT == 2 ? e8m0_to_f32(__ldg(args.rowmax[NMAT - 1] + (size_t)g * args.rows + row)) : 0.f;
-            if (!role_wait(smem_u32(tfull + acc), (tc >> 1) & 1, abort_flag, lim, args.status, 7)) break;
+            if (!role_wait(smem_u32(tfull + acc), (tc / NACC) & 1, abort_flag, lim, args.status, 7)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
             const int nchunks = (nrows + 15) >> 4;
@@ -386,7 +387,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                             const float rs = args.rscale ? __ldg(args.rscale + row0 + n) : 1.f;
                             const float gv = __uint_as_float(v0[j]) * fw0 * rs;
                             const float uv = __uint_as_float(v1[j]) * fw1 * rs;
-                            const float a = gv / (1.0f + expf(-gv)) * uv;
+                            const float a = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
                             if (!(fabsf(a) <= 65504.f)) set_status(args.status, K3MOE_ERR_RANGE, 2);
                             reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                         } else if (MODE == OUT_BF16) {
