@@ -211,4 +211,13 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, int bf16)
     return d;
 }
 
+// Hardware tanh approximation (PTX tanh.approx.f32; relative error about 2^-11),
+// used where the result is rounded to f16 anyway.
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace k3

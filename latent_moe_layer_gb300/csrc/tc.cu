@@ -40,7 +40,8 @@ bool encode_packed(CUtensorMap *m, const void *base, int rows, int cols)
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// f16 rows [rows, cols]: box 64 x bn, 128-byte swizzle.
+// f16 rows [rows, cols]: box 64 x bn rows, 128-byte swizzle (bn = 16: tiles load
+// only the 16-row boxes their rows need).
 bool encode_act(CUtensorMap *m, const void *base, int rows, int cols, int bn)
 {
     auto fn = encode_fn();
@@ -52,6 +53,11 @@ bool encode_act(CUtensorMap *m, const void *base, int rows, int cols, int bn)
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_act_maps(ActMaps *m, const void *base, int rows, int cols)
+{
+    return encode_act(&m->big, base, rows, cols, EX_BBIG) && encode_act(&m->small, base, rows, cols, EX_BBOX);
 }
 
 // rowmax[row] = max scale byte of the row; grid over (rows, groups).
@@ -137,7 +143,7 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
 }
 
 template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
-int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
+int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
@@ -155,12 +161,7 @@ int launch_expert(const CUtensorMap &bmap, const ExpertGemmArgs &a, int max_tile
 }
 
 // Tile shape by the token count per expert: small N for decode batches.
-int pick_bn(int T, int K, int E)
-{
-    const size_t R = (size_t)T * K;
-    if (R <= (size_t)E * 24) return 32;
-    return R >= (size_t)E * 512 ? 128 : 256;
-}
+int pick_bn(int T, int K, int E) { return ((size_t)T * K <= (size_t)E * 24) ? 32 : 256; }
 
 }  // namespace
 
@@ -334,13 +335,11 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 }
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
-// accumulator sets NACC).  N <= 32: gate/up 3/4/2/2 (176 KB smem), down 4/4/4/2 (144 KB);
-// N <= 128: gate/up 2/3/2/2 (176 KB), down 3/4/3/2 (160 KB); N <= 256: gate/up 2/2/2/1 (192 KB; 512 TMEM columns),
-// down 3/3/3/2 (192 KB).  bn selects the tile shape: 32 (tensor path at decode sizes, shared experts),
-// 128 (many tokens per expert: double-buffered accumulators overlap the GLU
-// epilogue with the next tile) or 256 (fewer tokens per expert: one dequantised
-// weight tile serves up to 256 tokens).
-static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUtensorMap &b2,
+// accumulator sets NACC).  N <= 32 (decode-size batches, shared experts at small T):
+// gate/up 3/4/2/2 (176 KB smem), down 4/4/4/2 (144 KB).  N <= 256: gate/up 2/3/2/1
+// (224 KB; 512 TMEM columns), down 3/4/3/2 (224 KB).  Activation loads are
+// latency-bound, so the spare shared memory goes to activation slots.
+static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool f32_add)
 {
@@ -348,22 +347,19 @@ static int expert_pair(k3moe_handle *h, int bn, const CUtensorMap &b1, const CUt
     const int ns = h->num_sms;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
-             : bn == 128 ? launch_expert<2, 128, 2, 3, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
-                         : launch_expert<2, 256, 2, 2, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
+        rc = bn == 32 ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
+                      : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
-        // the activation tensor map's box is bn rows: the kernel's BN must equal bn
+        // the tile list was cut at bn rows: the kernel's BN must equal bn
         if (f32_add)
-            rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
-                 : bn == 128 ? launch_expert<1, 128, 3, 4, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
-                             : launch_expert<1, 256, 3, 3, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
+                          : launch_expert<1, 256, 3, 4, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
         else
-            rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
-                 : bn == 128 ? launch_expert<1, 128, 3, 4, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
-                             : launch_expert<1, 256, 3, 3, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st);
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
+                          : launch_expert<1, 256, 3, 4, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
 }
@@ -391,8 +387,8 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         K3_CUDA_TRY(cudaGetLastError());
     }
     const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
-    CUtensorMap bm1, bm2;
-    if (!encode_act(&bm1, ws.hperm, R, L, bn) || !encode_act(&bm2, ws.act, R, I, bn)) return K3MOE_ERR_CUDA;
+    ActMaps bm1, bm2;
+    if (!encode_act_maps(&bm1, ws.hperm, R, L) || !encode_act_maps(&bm2, ws.act, R, I)) return K3MOE_ERR_CUDA;
     const uint8_t *rm = h->d_rowmax;
     ExpertGemmArgs a1 = {};
     a1.amaps = (const CUtensorMap *)h->d_tmaps;
@@ -485,8 +481,8 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
             k3_note_launch();
             K3_CUDA_TRY(cudaGetLastError());
         }
-        CUtensorMap sb1, sb2;
-        if (!encode_act(&sb1, ws.xs, T, H, sbn) || !encode_act(&sb2, ws.sact, T, S, sbn)) return K3MOE_ERR_CUDA;
+        ActMaps sb1, sb2;
+        if (!encode_act_maps(&sb1, ws.xs, T, H) || !encode_act_maps(&sb2, ws.sact, T, S)) return K3MOE_ERR_CUDA;
         const uint8_t *rs = rm + (size_t)E * (2 * I + L);
         ExpertGemmArgs s1 = a1;
         s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;

@@ -53,6 +53,14 @@ constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
 constexpr int EX_KP = 256;           // K per packed stage (128-byte FP4 rows)
 constexpr int EX_KS = 64;            // K per MMA sub-step (one 128-byte f16 row)
 constexpr int EX_NSUB = EX_KP / EX_KS;
+constexpr int EX_BBOX = 16;          // activation rows per small TMA box: a tile loads only the rows it needs,
+constexpr int EX_BBIG = 64;          // as 64-row boxes plus at most three 16-row boxes
+constexpr int EX_BBOX_BYTES = EX_BBOX * EX_KS * 2;
+
+// Tensor maps of one f16 activation matrix [rows, K] with 64- and 16-row boxes.
+struct ActMaps {
+    CUtensorMap big, small;
+};
 
 template <int NMAT, int BN, int NS, int NB, int NA>
 struct ExpertSmem {
@@ -103,7 +111,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
 
 template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
 __global__ void __launch_bounds__((8 + 4 * NMAT) * 32, 1)
-expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArgs args)
+expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     constexpr int EPI_WARP0 = 4 + 4 * NMAT;
@@ -190,11 +198,15 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
     } else if (warp == 2) {
         // ------------------------------------------------------------ TMA: activation sub-tiles
         if (lane == 0) {
-            prefetch_tmap(&bmap);
+            prefetch_tmap(&bmaps.big);
+            prefetch_tmap(&bmaps.small);
             const uint64_t pol_b = policy_evict_last();
             uint32_t bit = 0;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                const int row0 = __ldg(args.tiles + t / m_tiles).y;
+                const int4 tile = __ldg(args.tiles + t / m_tiles);
+                const int row0 = tile.y;
+                const int n16 = min(BN, max(16, (tile.z + 15) & ~15)) / EX_BBOX;    // = MMA N / 16
+                const int nbig = n16 / (EX_BBIG / EX_BBOX), nsmall = n16 % (EX_BBIG / EX_BBOX);
                 bool ok = true;
                 for (int ks = 0; ks < K / EX_KS; ++ks, ++bit) {
                     const int slot = bit % NB;
@@ -204,9 +216,14 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                         break;
                     }
                     const uint32_t fb = smem_u32(bfull + slot);
-                    mbar_expect_tx(fb, SM::B_BYTES);
-                    tma_load_2d_hint(smem_u32(smem + SM::OFF_B + slot * SM::B_BYTES), &bmap, fb, ks * EX_KS,
-                                     row0, pol_b);
+                    mbar_expect_tx(fb, n16 * EX_BBOX_BYTES);
+                    const uint32_t dst = smem_u32(smem + SM::OFF_B + slot * SM::B_BYTES);
+                    for (int b = 0; b < nbig; ++b)
+                        tma_load_2d_hint(dst + b * (EX_BBIG * EX_KS * 2), &bmaps.big, fb, ks * EX_KS,
+                                         row0 + b * EX_BBIG, pol_b);
+                    for (int b = 0; b < nsmall; ++b)
+                        tma_load_2d_hint(dst + nbig * (EX_BBIG * EX_KS * 2) + b * EX_BBOX_BYTES, &bmaps.small, fb,
+                                         ks * EX_KS, row0 + nbig * EX_BBIG + b * EX_BBOX, pol_b);
                 }
                 if (!ok) break;
             }
@@ -362,6 +379,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
         const int q = warp - EPI_WARP0;                    // TMEM lanes 32q .. 32q+31
         const int r = q * 32 + lane;
         uint32_t tc = 0;
+        bool bad = false;
         for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
             const int4 tile = __ldg(args.tiles + t / m_tiles);
             const int g = tile.x, row0 = tile.y, nrows = tile.z;
@@ -374,6 +392,13 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
             const int nchunks = (nrows + 15) >> 4;
             for (int c = 0; c < nchunks; ++c) {
+                // per-token factors first: their loads overlap the TMEM reads
+                float rs[16];
+                if (MODE == OUT_GLU_F16) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        rs[j] = (args.rscale && c * 16 + j < nrows) ? __ldg(args.rscale + row0 + c * 16 + j) : 1.f;
+                }
                 uint32_t v0[16], v1[16];
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
@@ -384,11 +409,11 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
                     if (n < nrows) {
                         const size_t orow = (size_t)(row0 + n);
                         if (MODE == OUT_GLU_F16) {
-                            const float rs = args.rscale ? __ldg(args.rscale + row0 + n) : 1.f;
-                            const float gv = __uint_as_float(v0[j]) * fw0 * rs;
-                            const float uv = __uint_as_float(v1[j]) * fw1 * rs;
-                            const float a = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
-                            if (!(fabsf(a) <= 65504.f)) set_status(args.status, K3MOE_ERR_RANGE, 2);
+                            // SiLU(gv) = gv * sigmoid(gv) = hv + hv * tanh(hv) with hv = gv / 2
+                            const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs[j]);
+                            const float uv = __uint_as_float(v1[j]) * (fw1 * rs[j]);
+                            const float a = fmaf(hv, tanh_approx(hv), hv) * uv;
+                            bad |= !(fabsf(a) <= 65504.f);
                             reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                         } else if (MODE == OUT_BF16) {
                             const float y = __uint_as_float(v0[j]) * fw0;
@@ -405,6 +430,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const ExpertGemmArg
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
         }
+        if (bad) set_status(args.status, K3MOE_ERR_RANGE, 2);
     }
 
     tc_fence_before();
