@@ -155,7 +155,7 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
         attr = true;
     }
     const int grid = max(1, min(num_sms, max_tiles));
-    kern<<<grid, (8 + 4 * NMAT) * 32, SM::BYTES, st>>>(bmap, a);
+    kern<<<grid, ex_threads(NMAT), SM::BYTES, st>>>(bmap, a);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

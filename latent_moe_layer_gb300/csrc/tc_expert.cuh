@@ -20,7 +20,8 @@
 //   warp 1            TMEM allocator and the single MMA-issuing thread
 //   warps 4..4+4*NMAT dequant: one thread per weight row, FP4 -> f16 into the
 //                     128-byte-swizzled K-major layout the MMA reads
-//   last 4 warps      epilogue: TMEM -> registers -> scaled outputs
+//   last 8 warps      epilogue: TMEM -> registers -> scaled outputs, two warps per
+//                     TMEM lane quarter taking alternate 16-token chunks
 // Every wait is bounded; on expiry the CTA records K3MOE_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
 #pragma once
@@ -71,8 +72,9 @@ struct ExpertSmem {
     static constexpr int OFF_B = OFF_A + NA * NMAT * A_BYTES;
     static constexpr int OFF_PK = OFF_B + NB * B_BYTES;
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
-    static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1;
-    static constexpr int BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;   // + tmem holder/flag + align slack
+    static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
+    static constexpr int OFF_RS = OFF_BAR + N_BAR * 8 + 16;          // after the tmem holder and abort flag
+    static constexpr int BYTES = OFF_RS + BN * 4 + 1024;              // + per-token factors + align slack
 };
 
 __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
@@ -109,8 +111,13 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
     }
 }
 
+// Threads per CTA: 4 control warps, 4 dequant warps per weight matrix, EX_NEPI
+// epilogue warps (two per TMEM lane quarter, alternating 16-token chunks).
+constexpr int EX_NEPI = 8;
+__host__ __device__ constexpr int ex_threads(int nmat) { return (4 + 4 * nmat + EX_NEPI) * 32; }
+
 template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
-__global__ void __launch_bounds__((8 + 4 * NMAT) * 32, 1)
+__global__ void __launch_bounds__(ex_threads(NMAT), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
@@ -127,7 +134,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
     uint64_t *bfull = pempty + NS, *bempty = bfull + NB;
     uint64_t *afull = bempty + NB, *aempty = afull + NA;
     uint64_t *tfull = aempty + NA, *tempty = tfull + 2, *drain = tempty + 2;
-    uint32_t *tmem_holder = (uint32_t *)(drain + 1);
+    uint64_t *rsfull = drain + 1, *rsempty = drain + 2;      // per-token factor staging (epilogue only)
+    uint32_t *tmem_holder = (uint32_t *)(drain + 3);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,9 +159,11 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(tfull + i), 1);
-            mbar_init(smem_u32(tempty + i), 4);
+            mbar_init(smem_u32(tempty + i), EX_NEPI);
         }
         mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(rsfull), EX_NEPI * 32);
+        mbar_init(smem_u32(rsempty), EX_NEPI);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -376,8 +386,11 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
         }
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp - EPI_WARP0;                    // TMEM lanes 32q .. 32q+31
+        const int q = warp & 3;                            // TMEM lanes 32q .. 32q+31
+        const int half = (warp - EPI_WARP0) >> 2;          // chunks c with c % 2 == half
+        const int eth = (warp - EPI_WARP0) * 32 + lane;
         const int r = q * 32 + lane;
+        float *srs = reinterpret_cast<float *>(smem + SM::OFF_RS);
         uint32_t tc = 0;
         bool bad = false;
         for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
@@ -387,18 +400,20 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             const int acc = (int)(tc % NACC);
             const float fw0 = e8m0_to_f32(__ldg(args.rowmax[0] + (size_t)g * args.rows + row));
             const float fw1 = NMAT == 2 ? e8m0_to_f32(__ldg(args.rowmax[NMAT - 1] + (size_t)g * args.rows + row)) : 0.f;
+            if (MODE == OUT_GLU_F16) {
+                // the tile's per-token factors, staged while its MMAs run, once
+                // the epilogue warps have finished with the previous tile's
+                if (tc > 0 && !role_wait(smem_u32(rsempty), (tc - 1) & 1, abort_flag, lim, args.status, 9)) break;
+                for (int i = eth; i < nrows; i += EX_NEPI * 32)
+                    srs[i] = args.rscale ? __ldg(args.rscale + row0 + i) : 1.f;
+                mbar_arrive(smem_u32(rsfull));
+                if (!role_wait(smem_u32(rsfull), tc & 1, abort_flag, lim, args.status, 9)) break;
+            }
             if (!role_wait(smem_u32(tfull + acc), (tc / NACC) & 1, abort_flag, lim, args.status, 7)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
             const int nchunks = (nrows + 15) >> 4;
-            for (int c = 0; c < nchunks; ++c) {
-                // per-token factors first: their loads overlap the TMEM reads
-                float rs[16];
-                if (MODE == OUT_GLU_F16) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        rs[j] = (args.rscale && c * 16 + j < nrows) ? __ldg(args.rscale + row0 + c * 16 + j) : 1.f;
-                }
+            for (int c = half; c < nchunks; c += 2) {
                 uint32_t v0[16], v1[16];
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
@@ -410,8 +425,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         const size_t orow = (size_t)(row0 + n);
                         if (MODE == OUT_GLU_F16) {
                             // SiLU(gv) = gv * sigmoid(gv) = hv + hv * tanh(hv) with hv = gv / 2
-                            const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs[j]);
-                            const float uv = __uint_as_float(v1[j]) * (fw1 * rs[j]);
+                            const float rs = srs[n];
+                            const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
+                            const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                             const float a = fmaf(hv, tanh_approx(hv), hv) * uv;
                             bad |= !(fabsf(a) <= 65504.f);
                             reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
@@ -428,7 +444,10 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
+            if (lane == 0) {
+                mbar_arrive(smem_u32(tempty + acc));
+                if (MODE == OUT_GLU_F16) mbar_arrive(smem_u32(rsempty));
+            }
         }
         if (bad) set_status(args.status, K3MOE_ERR_RANGE, 2);
     }
