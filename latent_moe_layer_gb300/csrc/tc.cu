@@ -336,9 +336,11 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
 // accumulator sets NACC).  N <= 32 (decode-size batches, shared experts at small T):
-// gate/up 3/4/2/2 (176 KB smem), down 4/4/4/2 (144 KB).  N <= 256: gate/up 2/3/2/1
-// (224 KB; 512 TMEM columns), down 3/4/3/2 (224 KB).  Activation loads are
-// latency-bound, so the spare shared memory goes to activation slots.
+// gate/up 3/4/2/2 (176 KB smem), down 4/4/4/2 (144 KB).  N <= 256: both 2/3/2/1
+// (224 KB; 512 TMEM columns), the down projection taking 256 weight rows per job
+// (two 128-row blocks against one activation tile, halving activation traffic).
+// Activation loads are latency-bound, so the spare shared memory goes to
+// activation slots.
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool f32_add)
@@ -356,10 +358,10 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
         // the tile list was cut at bn rows: the kernel's BN must equal bn
         if (f32_add)
             rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
-                          : launch_expert<1, 256, 3, 4, 3, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
+                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
         else
             rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
-                          : launch_expert<1, 256, 3, 4, 3, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st);
+                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
 }

@@ -140,7 +140,11 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = args.K, nkp = K / EX_KP;
-    const int m_tiles = args.rows / EX_BM;
+    // GLU: the two matrices share the job's 128 rows.  Otherwise NMAT = 2 takes two
+    // 128-row blocks of the same matrix, so each activation tile feeds 256 rows.
+    constexpr bool ROWPAIR = MODE != OUT_GLU_F16 && NMAT == 2;
+    constexpr int JOB_ROWS = ROWPAIR ? 2 * EX_BM : EX_BM;
+    const int m_tiles = args.rows / JOB_ROWS;
     const int total = __ldg(args.n_tiles) * m_tiles;
     const uint32_t lim = args.spin_limit;
 
@@ -183,7 +187,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             uint32_t pit = 0;
             for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
                 const int4 tile = __ldg(args.tiles + t / m_tiles);
-                const int g = tile.x, m0 = (t % m_tiles) * EX_BM;
+                const int g = tile.x, m0 = (t % m_tiles) * JOB_ROWS;
                 const CUtensorMap *am0 = args.amaps + (size_t)g * args.amap_stride + args.amap_off[0];
                 const CUtensorMap *am1 = args.amaps + (size_t)g * args.amap_stride + args.amap_off[NMAT - 1];
                 bool ok = true;
@@ -199,7 +203,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                     uint8_t *pk = smem + SM::OFF_PK + slot * NMAT * SM::PK_BYTES;
                     tma_load_2d_hint(smem_u32(pk), am0, fb, s * (EX_KP / 2), m0, pol_w);
                     if (NMAT == 2)
-                        tma_load_2d_hint(smem_u32(pk + SM::PK_BYTES), am1, fb, s * (EX_KP / 2), m0, pol_w);
+                        tma_load_2d_hint(smem_u32(pk + SM::PK_BYTES), am1, fb, s * (EX_KP / 2),
+                                         m0 + (ROWPAIR ? EX_BM : 0), pol_w);
                 }
                 if (!ok) break;
             }
@@ -298,7 +303,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
         uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = sc_cur;
         if (t < total) {
             const int4 tile = __ldg(args.tiles + t / m_tiles);
-            const int row = (t % m_tiles) * EX_BM + r;
+            const int row = (t % m_tiles) * JOB_ROWS + (ROWPAIR ? mat * EX_BM : 0) + r;
             emax = __ldg(args.rowmax[mat] + (size_t)tile.x * args.rows + row);
             srow = args.scales[mat][tile.x] + (size_t)row * kblk;
             sc_cur = __ldg(reinterpret_cast<const uint4 *>(srow));
@@ -308,7 +313,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             const uint8_t *srow_next = nullptr;
             if (tn < total) {
                 const int4 tile = __ldg(args.tiles + tn / m_tiles);
-                const int row = (tn % m_tiles) * EX_BM + r;
+                const int row = (tn % m_tiles) * JOB_ROWS + (ROWPAIR ? mat * EX_BM : 0) + r;
                 srow_next = args.scales[mat][tile.x] + (size_t)row * kblk;
                 emax_next = __ldg(args.rowmax[mat] + (size_t)tile.x * args.rows + row);
             }
@@ -396,10 +401,11 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
         for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
             const int4 tile = __ldg(args.tiles + t / m_tiles);
             const int g = tile.x, row0 = tile.y, nrows = tile.z;
-            const int m0 = (t % m_tiles) * EX_BM, row = m0 + r;
+            const int m0 = (t % m_tiles) * JOB_ROWS, row = m0 + r;
+            const int row1 = row + (ROWPAIR ? EX_BM : 0);          // output row of matrix slot 1
             const int acc = (int)(tc % NACC);
             const float fw0 = e8m0_to_f32(__ldg(args.rowmax[0] + (size_t)g * args.rows + row));
-            const float fw1 = NMAT == 2 ? e8m0_to_f32(__ldg(args.rowmax[NMAT - 1] + (size_t)g * args.rows + row)) : 0.f;
+            const float fw1 = NMAT == 2 ? e8m0_to_f32(__ldg(args.rowmax[NMAT - 1] + (size_t)g * args.rows + row1)) : 0.f;
             if (MODE == OUT_GLU_F16) {
                 // the tile's per-token factors, staged while its MMAs run, once
                 // the epilogue warps have finished with the previous tile's
@@ -432,12 +438,13 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                             bad |= !(fabsf(a) <= 65504.f);
                             reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                         } else if (MODE == OUT_BF16) {
-                            const float y = __uint_as_float(v0[j]) * fw0;
-                            reinterpret_cast<uint16_t *>(args.out)[orow * args.rows + row] = f32_to_bf16(y);
+                            uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
+                            o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
+                            if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * fw1);
                         } else {
-                            const float y = __uint_as_float(v0[j]) * fw0;
-                            float *o = reinterpret_cast<float *>(args.out) + orow * args.rows + row;
-                            *o += y;
+                            float *o = reinterpret_cast<float *>(args.out) + orow * args.rows;
+                            o[row] += __uint_as_float(v0[j]) * fw0;
+                            if (ROWPAIR) o[row1] += __uint_as_float(v1[j]) * fw1;
                         }
                     }
                 }
