@@ -60,10 +60,10 @@ __device__ __forceinline__ void decode8(uint32_t w, __half2 sc, uint32_t (&o)[4]
 
 __device__ __forceinline__ __half2 pow2_h2(int d)
 {
-    // 2^d (d <= 0) as f16x2: subnormals below 2^-14, zero below 2^-24
-    const uint32_t b = d >= -14 ? (uint32_t)(d + 15) << 10 : (d >= -24 ? 1u << (d + 24) : 0u);
-    const uint32_t bb = b | (b << 16);
-    return *reinterpret_cast<const __half2 *>(&bb);
+    // 2^d (d <= 0) as f16x2: built exactly in fp32 (d clamped at -126, far below
+    // f16's range) and rounded once to f16 -- subnormals below 2^-14, zero below 2^-24
+    const float f = __int_as_float((max(d, -126) + 127) << 23);
+    return __float2half2_rn(f);
 }
 
 // Packed FP4 rows arrive by TMA (per-expert tensor maps: 128 rows x 128 bytes
@@ -211,10 +211,12 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                     uint4 hb[2][2];
 #pragma unroll
                     for (int nb = 0; nb < 2; ++nb) {
-                        const int br = 8 * nb + g8;
-                        const uint8_t *bx = bbase + ks * 16 * 128 + br * 128;
-                        hb[nb][0] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c) ^ (br & 7)));
-                        hb[nb][1] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c + 1) ^ (br & 7)));
+                        if (nb < nnb) {                  // tokens 8..15 only when the tile has them
+                            const int br = 8 * nb + g8;
+                            const uint8_t *bx = bbase + ks * 16 * 128 + br * 128;
+                            hb[nb][0] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c) ^ (br & 7)));
+                            hb[nb][1] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c + 1) ^ (br & 7)));
+                        }
                     }
                     if (ks == 3) {
                         fence_proxy_async_smem();

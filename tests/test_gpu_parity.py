@@ -72,6 +72,21 @@ def test_small_aligned_parity(path, name, T):
     assert_parity(compare(cfg, g, ref))
 
 
+@pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
+@pytest.mark.parametrize("T", [40, 300], ids=["decode_tiles", "tcgen05_tiles"])
+def test_wide_scale_exponents(path, T):
+    # E8M0 exponents uniform over 96..126: a row's blocks sit up to 30 binary
+    # orders below its largest, so the fast paths' exact f16 decode meets its
+    # normal, subnormal (below 2^-14) and flushed (below 2^-24) ranges
+    d = dict(synth.SMALL_SHARED.__dict__)
+    d.update(name="small_shared_wide_exp", wseed=12, exp_lo=96, exp_hi=126)
+    cfg = synth.LayerConfig(**d).with_tokens(T)
+    g = run_gpu(cfg, path)
+    assert g["status"] == 0
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
 def test_tensor_and_generic_paths_agree():
     cfg = synth.SMALL_SHARED.with_tokens(64)
     a = run_gpu(cfg, GEN)
