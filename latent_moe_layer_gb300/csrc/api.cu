@@ -333,6 +333,9 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->stage_out = cv.take<uint16_t>(Tn * c.hidden);
     ws->stage_idx = cv.take<int32_t>(R + 1);
     ws->stage_w = cv.take<float>(R + 1);
+    ws->chunk_cnt = cv.take<int32_t>(T >= K3_PERM_CHUNKED_T
+                                         ? (size_t)c.n_experts * ((T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK)
+                                         : 1);
     ws->bytes = align_up(cv.off, 256);
     return K3MOE_OK;
 }

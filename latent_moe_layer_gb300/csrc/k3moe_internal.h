@@ -148,8 +148,14 @@ struct k3_ws {
     uint16_t *stage_out;  // [T, H]
     int32_t *stage_idx;   // [T, K]
     float *stage_w;       // [T, K]
+    int32_t *chunk_cnt;   // [E, ceil(T / K3_PERM_CHUNK)] per-chunk counts, then bases (large T)
     size_t bytes;
 };
+
+// Token permutation: from K3_PERM_CHUNKED_T tokens on, a chunked stable scatter
+// (tokens in chunks of K3_PERM_CHUNK) replaces the one-CTA-per-expert scan.
+constexpr int K3_PERM_CHUNK = 32;
+constexpr int K3_PERM_CHUNKED_T = 512;
 
 int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base may be NULL (sizing)
 

@@ -208,6 +208,92 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t *__rest
     }
 }
 
+// ---- chunked stable permutation (large T).  A token selects an expert at most
+// once, so the stable (t, k) order within an expert's segment is token order:
+// a row's position is the expert's offset, plus the expert's count in earlier
+// chunks, plus its count at earlier tokens of the same chunk.
+
+// Per-chunk expert counts, expert-major [E][nch], and the totals.
+__global__ void __launch_bounds__(256) perm_chunk_count_kernel(const int32_t *__restrict__ idx, int T, int K,
+                                                               int E, int nch, int32_t *__restrict__ chunk_cnt,
+                                                               int32_t *__restrict__ counts, int *status)
+{
+    extern __shared__ int cnt[];                     // [E]
+    const int ch = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int p0 = ch * K3_PERM_CHUNK * K, p1 = min(T, (ch + 1) * K3_PERM_CHUNK) * K;
+    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+        const int e = idx[p];
+        if (e < 0 || e >= E) {
+            set_status(status, K3MOE_ERR_RANGE, e);
+            continue;
+        }
+        atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int v = cnt[e];
+        chunk_cnt[(size_t)e * nch + ch] = v;
+        if (v) atomicAdd(counts + e, v);
+    }
+}
+
+// One CTA per expert: chunk counts -> chunk bases (offset + exclusive scan over chunks).
+__global__ void __launch_bounds__(1024) perm_chunk_base_kernel(int nch, const int32_t *__restrict__ offsets,
+                                                               int32_t *__restrict__ chunk_cnt)
+{
+    __shared__ int s[1024];
+    __shared__ int carry;
+    const int e = blockIdx.x, tid = threadIdx.x;
+    int32_t *row = chunk_cnt + (size_t)e * nch;
+    if (tid == 0) carry = offsets[e];
+    __syncthreads();
+    for (int c0 = 0; c0 < nch; c0 += 1024) {
+        const int c = c0 + tid;
+        const int v = c < nch ? row[c] : 0;
+        s[tid] = v;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {     // inclusive Hillis-Steele scan
+            const int a = tid >= off ? s[tid - off] : 0;
+            __syncthreads();
+            s[tid] += a;
+            __syncthreads();
+        }
+        if (c < nch) row[c] = carry + s[tid] - v;
+        __syncthreads();
+        if (tid == 1023) carry += s[1023];
+        __syncthreads();
+    }
+}
+
+// One warp per chunk: the chunk's tokens in order, lane k placing (t, k).
+__global__ void __launch_bounds__(32) perm_chunk_scatter_kernel(const int32_t *__restrict__ idx, int T, int K,
+                                                                int E, int nch,
+                                                                const int32_t *__restrict__ chunk_base,
+                                                                int32_t *__restrict__ tok_of,
+                                                                int32_t *__restrict__ row_of)
+{
+    extern __shared__ int next[];                    // [E] next free row per expert
+    const int ch = blockIdx.x, lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32) next[e] = chunk_base[(size_t)e * nch + ch];
+    __syncwarp();
+    const int t1 = min(T, (ch + 1) * K3_PERM_CHUNK);
+    for (int t = ch * K3_PERM_CHUNK; t < t1; ++t) {
+        if (lane < K) {
+            const int p = t * K + lane;
+            const int e = idx[p];
+            if (e >= 0 && e < E) {                   // the experts of one token are distinct
+                const int row = next[e];
+                next[e] = row + 1;
+                tok_of[row] = t;
+                row_of[p] = row;
+            }
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace k3
 
 using namespace k3;
@@ -232,12 +318,27 @@ int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n,
 {
     const int E = h->cfg.n_experts, K = h->cfg.top_k, n = T * K;
     K3_CUDA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int32_t) * E, st));
-    perm_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(ws.idx, n, E, ws.counts, h->d_status);
+    const bool chunked = T >= K3_PERM_CHUNKED_T;
+    const int nch = (T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK;
+    const size_t esm = sizeof(int) * E;              // E <= 1024: 4 KB of shared memory
+    if (chunked) {
+        perm_chunk_count_kernel<<<nch, 256, esm, st>>>(ws.idx, T, K, E, nch, ws.chunk_cnt, ws.counts,
+                                                       h->d_status);
+    } else {
+        perm_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(ws.idx, n, E, ws.counts, h->d_status);
+    }
     k3_note_launch();
     perm_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, E, tile_n, ws.offsets, ws.active,
                                          reinterpret_cast<int4 *>(ws.tiles), ws.meta);
     k3_note_launch();
-    perm_scatter_kernel<<<E, 256, 0, st>>>(ws.idx, n, K, ws.counts, ws.offsets, ws.tok_of, ws.row_of);
+    if (chunked) {
+        perm_chunk_base_kernel<<<E, 1024, 0, st>>>(nch, ws.offsets, ws.chunk_cnt);
+        k3_note_launch();
+        perm_chunk_scatter_kernel<<<nch, 32, esm, st>>>(ws.idx, T, K, E, nch, ws.chunk_cnt, ws.tok_of,
+                                                        ws.row_of);
+    } else {
+        perm_scatter_kernel<<<E, 256, 0, st>>>(ws.idx, n, K, ws.counts, ws.offsets, ws.tok_of, ws.row_of);
+    }
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

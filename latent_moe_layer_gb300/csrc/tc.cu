@@ -142,12 +142,12 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
     if (threadIdx.x == 0) *count = n;
 }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
 int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
-    using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
-    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE, ATMEM>;
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
@@ -155,7 +155,7 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
         attr = true;
     }
     const int grid = max(1, min(num_sms, max_tiles));
-    kern<<<grid, ex_threads(NMAT, ATMEM), SM::BYTES, st>>>(bmap, a);
+    kern<<<grid, ex_threads(NMAT), SM::BYTES, st>>>(bmap, a);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
@@ -335,11 +335,8 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 }
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
-// accumulator sets NACC).  N <= 32 (decode-size batches, shared experts at small T):
-// the decoded A sub-tiles go to TMEM instead of shared memory, so the packed ring
-// is deep -- gate/up 5/8/4/2 (192 KB smem, 384 TMEM columns), down 8/8/4/2 (160 KB,
-// 192 columns) -- and the kernel streams the touched experts' bytes from HBM
-// with little per-byte instruction work.  N <= 256: both 2/3/2/1
+// accumulator sets NACC).  N <= 32 (shared experts at small T): gate/up 3/4/2/2
+// (176 KB smem), down 4/4/4/2 (144 KB).  N <= 256: both 2/3/2/1
 // (224 KB; 512 TMEM columns), the down projection taking 256 weight rows per job
 // (two 128-row blocks against one activation tile, halving activation traffic).
 // Activation loads are latency-bound, so the spare shared memory goes to
@@ -352,7 +349,7 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
     const int ns = h->num_sms;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32 ? launch_expert<2, 32, 5, 8, 4, 2, OUT_GLU_F16, true>(b1, a1, max_tiles1, ns, st)
+        rc = bn == 32 ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
                       : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
     }
@@ -360,10 +357,10 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
         k3_stage sg(h, stage2, st);
         // the tile list was cut at bn rows: the kernel's BN must equal bn
         if (f32_add)
-            rc = bn == 32 ? launch_expert<1, 32, 8, 8, 4, 2, OUT_F32_ADD, true>(b2, a2, max_tiles2, ns, st)
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
                           : launch_expert<2, 256, 2, 3, 2, 1, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
         else
-            rc = bn == 32 ? launch_expert<1, 32, 8, 8, 4, 2, OUT_BF16, true>(b2, a2, max_tiles2, ns, st)
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
                           : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
@@ -381,11 +378,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         k3_stage sg(h, K3MOE_STAGE_TOPK, st);
         if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
     }
-#ifdef K3_DECODE_TMEM_A
-    const bool gemv = false;
-#else
     const bool gemv = bn == 32;     // routed experts at decode sizes: the streaming GEMV
-#endif
     {   // token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
         k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
         if ((rc = k3_launch_permute(h, ws, T, gemv ? 16 : bn, st))) return rc;

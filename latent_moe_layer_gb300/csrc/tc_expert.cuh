@@ -63,13 +63,13 @@ struct ActMaps {
     CUtensorMap big, small;
 };
 
-template <int NMAT, int BN, int NS, int NB, int NA, bool ATMEM = false>
+template <int NMAT, int BN, int NS, int NB, int NA>
 struct ExpertSmem {
     static constexpr int PK_BYTES = EX_BM * EX_KP / 2;      // 16384 packed bytes per matrix
     static constexpr int B_BYTES = BN * EX_KS * 2;          // activation sub-tile
     static constexpr int A_BYTES = EX_BM * EX_KS * 2;       // 16384 f16 tile
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + (ATMEM ? 0 : NA * NMAT * A_BYTES);   // ATMEM: A lives in TMEM
+    static constexpr int OFF_B = OFF_A + NA * NMAT * A_BYTES;
     static constexpr int OFF_PK = OFF_B + NB * B_BYTES;
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
     static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
@@ -111,29 +111,20 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
     }
 }
 
-// Threads per CTA: 4 control warps; dequant warps, per weight matrix 4 (one thread
-// per weight row) or, with ATMEM, 8 (two warps per row quarter taking alternate
-// 64-K sub-steps: decode-size tiles need the extra warps to hide latency); and
-// epilogue warps, 8 for the large tiles (two per TMEM lane quarter on alternate
-// 16-token chunks) or 4 with ATMEM.
-__host__ __device__ constexpr int ex_dqw(bool atmem) { return atmem ? 8 : 4; }
-__host__ __device__ constexpr int ex_nepi(bool atmem) { return atmem ? 4 : 8; }
-__host__ __device__ constexpr int ex_threads(int nmat, bool atmem)
-{
-    return (4 + ex_dqw(atmem) * nmat + ex_nepi(atmem)) * 32;
-}
+// Threads per CTA: 4 control warps, 4 dequant warps per weight matrix (one thread
+// per weight row) and 8 epilogue warps (two per TMEM lane quarter, alternating
+// 16-token chunks).
+constexpr int EX_NEPI = 8;
+__host__ __device__ constexpr int ex_threads(int nmat) { return (4 + 4 * nmat + EX_NEPI) * 32; }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
-__global__ void __launch_bounds__(ex_threads(NMAT, ATMEM), 1)
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
+__global__ void __launch_bounds__(ex_threads(NMAT), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
-    using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
-    constexpr int DQW = ex_dqw(ATMEM), NEPI = ex_nepi(ATMEM);
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
+    constexpr int DQW = 4, NEPI = EX_NEPI;
     constexpr int EPI_WARP0 = 4 + DQW * NMAT;
-    // TMEM columns: NACC accumulator sets (2: the epilogue overlaps the next tile),
-    // then with ATMEM the NA x NMAT decoded A sub-tiles (128 lanes x 32 columns each)
-    constexpr int ACOL0 = NACC * NMAT * BN;
-    constexpr int COLS = ACOL0 + (ATMEM ? NA * NMAT * EX_KS / 2 : 0);
+    constexpr int COLS = NACC * NMAT * BN;       // NACC accumulator sets (2: epilogue overlaps the next tile)
     constexpr uint32_t TMEM_COLS = (COLS <= 32) ? 32 : (COLS <= 64) ? 64 : (COLS <= 128) ? 128
                                  : (COLS <= 256) ? 256 : 512;
     static_assert(COLS <= 512 && (NACC == 1 || NACC == 2), "TMEM columns");
@@ -281,20 +272,12 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + SM::OFF_B + bslot * SM::B_BYTES));
 #pragma unroll
                     for (int mt = 0; mt < NMAT; ++mt) {
-                        if (ATMEM) {
-                            const uint32_t acol = tmem + ACOL0 + (aslot * NMAT + mt) * (EX_KS / 2);
+                        const uint64_t adesc =
+                            smem_desc_sw128(smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES));
 #pragma unroll
-                            for (int kk = 0; kk < EX_KS / 16; ++kk)   // 16 K = 8 columns
-                                tc_mma_f16_ts(dcol + mt * BN, acol + 8 * kk, bdesc + 2 * kk, idesc,
-                                              (ks > 0 || kk > 0) ? 1u : 0u);
-                        } else {
-                            const uint64_t adesc =
-                                smem_desc_sw128(smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES));
-#pragma unroll
-                            for (int kk = 0; kk < EX_KS / 16; ++kk)
-                                tc_mma_f16(dcol + mt * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                           (ks > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < EX_KS / 16; ++kk)
+                            tc_mma_f16(dcol + mt * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                       (ks > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(bempty + bslot));
                     tc_commit(smem_u32(aempty + aslot));
@@ -310,9 +293,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
         // ------------------------------------------------------------ dequant FP4 -> f16
         const int d = warp - 4;
         const int mat = d / DQW;
-        const int sub = d % DQW;
-        const int r = (sub % 4) * 32 + lane;               // weight row within the tile (lane quarter = warp % 4)
-        const int phase = sub / 4;                         // DQW = 8: decodes the sub-steps q with q % 2 == phase
+        const int r = (d % DQW) * 32 + lane;               // weight row within the tile
         const int kblk = K / 32;
         uint32_t pit = 0, ait = 0;
         // 16 scale bytes cover two packed stages; the next group is read one
@@ -352,14 +333,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 }
                 // the row's 128 packed bytes (128-byte swizzle of the TMA box)
                 const uint8_t *pk = smem + SM::OFF_PK + (slot * NMAT + mat) * SM::PK_BYTES + r * 128;
-                // DQW = 4: all eight 16-byte chunks; DQW = 8: chunks 2q, 2q+1 of this warp's sub-steps
-                constexpr int NC = DQW == 8 ? 4 : 8;
-                uint4 c[NC];
+                uint4 c[8];
 #pragma unroll
-                for (int j = 0; j < NC; ++j) {
-                    const int ch = DQW == 8 ? 4 * (j >> 1) + 2 * phase + (j & 1) : j;
-                    c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (ch ^ (r & 7)));
-                }
+                for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (j ^ (r & 7)));
                 // the stage is refilled by TMA (async proxy): order these generic reads before it
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -368,7 +344,6 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 const uint32_t sw_hi = (s & 1) ? sc_cur.w : sc_cur.y;
 #pragma unroll
                 for (int q = 0; q < EX_NSUB; ++q, ++ait) {
-                    if (DQW == 8 && (q & 1) != phase) continue;
                     const uint32_t sw32 = q < 2 ? sw_lo : sw_hi;
                     const int e0 = (sw32 >> (16 * (q & 1))) & 0xFF, e1 = (sw32 >> (16 * (q & 1) + 8)) & 0xFF;
                     const uint32_t f0 = f16_pow2_bits(e0 - emax), f1 = f16_pow2_bits(e1 - emax);
@@ -383,10 +358,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         break;
                     }
                     uint8_t *arow = smem + SM::OFF_A + (aslot * NMAT + mat) * SM::A_BYTES + r * 128;
-                    const uint4 lo = c[DQW == 8 ? 2 * (q >> 1) : 2 * q], hi = c[DQW == 8 ? 2 * (q >> 1) + 1 : 2 * q + 1];
+                    const uint4 lo = c[2 * q], hi = c[2 * q + 1];
                     const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                    uint32_t tv[ATMEM ? 32 : 1];                 // ATMEM: the row's 64 values, K order
-                    if (ATMEM) tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         uint32_t h0, h1, h2, h3;
@@ -405,26 +378,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         v.y = *reinterpret_cast<uint32_t *>(&q1);
                         v.z = *reinterpret_cast<uint32_t *>(&q2);
                         v.w = *reinterpret_cast<uint32_t *>(&q3);
-                        if (ATMEM) {
-                            tv[(4 * j + 0) % (ATMEM ? 32 : 1)] = v.x;
-                            tv[(4 * j + 1) % (ATMEM ? 32 : 1)] = v.y;
-                            tv[(4 * j + 2) % (ATMEM ? 32 : 1)] = v.z;
-                            tv[(4 * j + 3) % (ATMEM ? 32 : 1)] = v.w;
-                        } else {
-                            *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
-                        }
+                        *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
                     }
-                    if (ATMEM) {
-                        // lanes 32 (warp % 4) .. +31 = rows r of this warp; columns of A slot (aslot, mat)
-                        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + ACOL0 +
-                                            (aslot * NMAT + mat) * (EX_KS / 2);
-                        tmem_st16(ta, tv);
-                        tmem_st16(ta + 16, tv + (ATMEM ? 16 : 0));
-                        tc_wait_st();
-                        tc_fence_before();
-                    } else {
-                        fence_proxy_async_smem();
-                    }
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(afull + aslot));
                 }
@@ -438,7 +394,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                            // TMEM lanes 32q .. 32q+31
-        const int half = (warp - EPI_WARP0) >> 2;          // NEPI = 8: chunks c with c % 2 == half
+        const int half = (warp - EPI_WARP0) >> 2;          // chunks c with c % 2 == half
         const int eth = (warp - EPI_WARP0) * 32 + lane;
         const int r = q * 32 + lane;
         float *srs = reinterpret_cast<float *>(smem + SM::OFF_RS);

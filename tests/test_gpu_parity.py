@@ -51,7 +51,7 @@ def test_tiny_t8_full_parity():
     assert_parity(compare(cfg, g, ref))
 
 
-@pytest.mark.parametrize("T", [1, 3, 17, 100, 333])
+@pytest.mark.parametrize("T", [1, 3, 17, 100, 333, 1000])   # 1000: chunked permutation, ragged last chunk
 def test_tiny_ragged_token_counts(T):
     cfg = synth.CONFIGS[0].with_tokens(T)
     g = run_gpu(cfg, GEN)
@@ -62,6 +62,7 @@ def test_tiny_ragged_token_counts(T):
 
 @pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
 @pytest.mark.parametrize("name,T", [("SMALL_ALIGNED", 40), ("SMALL_ALIGNED", 7), ("SMALL_ALIGNED", 300),
+                                    ("SMALL_ALIGNED", 700),
                                     ("SMALL_SHARED", 40), ("SMALL_SHARED", 150)])
 def test_small_aligned_parity(path, name, T):
     cfg = getattr(synth, name).with_tokens(T)
