@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per touched expert per launch, from the ncu capture in
 # profiles/gemv_expert_decode_dram.md (decode GEMV, 128-expert case, scaled by
 # touched experts).  Valid only while those kernels are unchanged.
-NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.15e6, ("expert_down", "gemv"): 5.874e6}
+NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.16e6, ("expert_down", "gemv"): 5.871e6}
 
 
 def peaks():
@@ -131,8 +131,9 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
-def oracle_sample_time(cfg, n_tokens, seed=0):
-    """Time the fp64 oracle on a fixed token sample; returns (seconds, tokens, threads)."""
+def oracle_sample_time(cfg, n_tokens, seed=0, min_seconds=0.0):
+    """Time the fp64 oracle on a fixed token sample, repeated until at least
+    min_seconds have elapsed; returns (seconds, tokens processed, threads)."""
     import numpy as np
     from latent_moe_layer_gb300 import synth
     from oracle import oracle
@@ -143,9 +144,14 @@ def oracle_sample_time(cfg, n_tokens, seed=0):
     idx, _, _, _ = oracle.route(cfg, dense, x)
     experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
     t0 = time.perf_counter()
-    oracle.forward(cfg, dense, experts, x)
-    dt = time.perf_counter() - t0
-    return dt, len(rows), oracle.max_threads()
+    reps = 0
+    while True:
+        oracle.forward(cfg, dense, experts, x)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return dt, reps * len(rows), oracle.max_threads()
 
 
 def cpu_sample_size(config_id):
@@ -201,6 +207,8 @@ def run_ours(args):
     if args.experts:
         # reduced expert count: for profiler captures that must stay a few GB on the device
         cfg = synth.LayerConfig(**{**cfg.__dict__, "E": args.experts, "name": cfg.name + f"_E{args.experts}"})
+    if args.tokens:
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "T": args.tokens, "name": cfg.name + f"_T{args.tokens}"})
     pk, pk_src = peaks()
 
     dw = k3moe.DeviceWeights(cfg)
@@ -301,9 +309,10 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = cpu_sample_size(args.config)
-        dt, nt, thr = oracle_sample_time(cfg, n)
+        dt, nt, thr = oracle_sample_time(cfg, n, min_seconds=10.0)
         cpu = {"value": round(nt / dt, 4), "unit": "tokens/s", "cores": thr, "kind": "oracle",
-               "sample": f"{nt} tokens of {cfg.name} (fp64 oracle, all layer steps), {dt:.2f} s"}
+               "sample": f"{n} tokens of {cfg.name} (fp64 oracle, all layer steps), repeated to "
+                         f"{nt} tokens in {dt:.2f} s"}
 
     exp_ms = stage_ms["gate_up"] + stage_ms["expert_down"]
     detail = {
@@ -382,6 +391,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling aid)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling aid)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

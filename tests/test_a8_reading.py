@@ -1,0 +1,135 @@
+"""The A8 option, measured on the CPU: MXFP8 activations against the exact layer.
+
+The K3 report review (sections on deployment-aware post-training and on the
+open weights) says the routed experts were trained and are shipped with MXFP4
+weights and MXFP8 input activations.  The layer's definition, which the parity
+bar is stated against, has no activation rounding.  This module measures what
+rounding the expert GEMMs' two activation inputs (the latent h, and the GLU
+output a) to MXFP8 would cost against that definition, using the fp64 oracle
+for everything else.
+
+MXFP8 follows the OCP Microscaling v1.0 definition: E4M3 elements (bias 7, 3
+mantissa bits, subnormal spacing 2^-9, largest finite 448, conversion
+saturating), one E8M0 scale per 32 elements, scale = 2^(floor(log2 amax) - 8)
+(8 = E4M3's largest exponent).
+"""
+import numpy as np
+import pytest
+
+from latent_moe_layer_gb300 import synth
+from oracle import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ------------------------------------------------------------------ MXFP8 (test-local)
+def e4m3_round(v):
+    """Round to the nearest E4M3 value (ties to even), saturating at +-448."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                      # below 2^-6 the spacing stays 2^-9 (subnormals)
+    step = np.exp2(e - 3)
+    q = np.rint(a / step) * step               # numpy rint: ties to even
+    q = np.minimum(q, 448.0)
+    return np.sign(v) * q
+
+
+def e4m3_grid():
+    """All finite non-negative E4M3 values, from the bit layout (s eeee mmm)."""
+    vals = []
+    for code in range(0x7F):                   # 0x7F is NaN
+        e, m = code >> 3, code & 7
+        vals.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def mxfp8(x, no_clip=False):
+    """Quantise the last axis in blocks of 32 to E4M3 x 2^X (X shared per block).
+
+    X = floor(log2 amax) - 8 (the OCP rule; the block maximum may saturate), or
+    with ``no_clip`` the smallest X with amax / 2^X <= 448."""
+    x = np.asarray(x, np.float64)
+    b = x.reshape(*x.shape[:-1], -1, 32)
+    amax = np.abs(b).max(axis=-1, keepdims=True)
+    safe = np.where(amax > 0, amax, 1.0)
+    X = np.ceil(np.log2(safe / 448.0)) if no_clip else np.floor(np.log2(safe)) - 8
+    X = np.clip(X, -127, 127)
+    s = np.exp2(X)
+    return (e4m3_round(b / s) * s).reshape(x.shape)
+
+
+def test_e4m3_rounding_pins():
+    g = e4m3_grid()
+    assert g.max() == 448.0 and g[1] == 2.0 ** -9 and g[8] == 2.0 ** -6
+    assert np.array_equal(e4m3_round(g), g) and np.array_equal(e4m3_round(-g), -g)
+    assert e4m3_round(500.0) == 448.0                     # saturating conversion
+    assert e4m3_round(1 + 2 ** -4) == 1.0                 # tie -> even mantissa
+    assert e4m3_round(1 + 3 * 2 ** -4) == 1.25            # tie -> even mantissa (up)
+    assert e4m3_round(2.0 ** -10) == 0.0                  # half the smallest subnormal -> 0
+    r = np.random.default_rng(0).standard_normal(4096) * 10
+    q = e4m3_round(r)
+    assert np.all(np.isin(np.abs(q), g))
+    # nearest: no grid point strictly closer than the chosen one
+    d = np.abs(np.abs(r)[:, None] - g[None, :]).min(axis=1)
+    assert np.allclose(np.abs(np.abs(r) - np.abs(q)), d)
+
+
+def test_mxfp8_block_scale():
+    x = np.zeros(64)
+    x[3], x[40], x[41], x[42] = 3.0, -1000.0, 0.3, 0.01
+    q = mxfp8(x)
+    assert q[3] == 3.0                  # block amax 3: X = 2^(1 - 8), 3 = 384 x 2^-7 exactly
+    assert q[40] == -896.0              # block amax 1000: X = 2^(9 - 8), 500 saturates to 448
+    assert q[41] == 0.3125              # 0.15 -> 10 x 2^-6 (normal, spacing 2^-6), x 2
+    assert q[42] == 3 * 2.0 ** -9 * 2   # 0.005 -> 3 x 2^-9 (subnormal), x 2
+    assert np.all(q[np.r_[0:3, 4:32]] == 0)
+
+
+# ------------------------------------------------------------------ the layer, re-stated with hooks
+def _bf16(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _layer_from_latent(cfg, dense, experts, h, idx, w, quant):
+    """Experts, combine, RMSNorm and up-projection in fp64 from the oracle's latent
+    h, indices and weights; ``quant`` is applied to each expert GEMM's input."""
+    up, gamma = _bf16(dense.w_up), _bf16(dense.gamma)
+    deq = {e: [oracle.dequant(p, s) for p, s in mats] for e, mats in experts.items()}
+    out = np.zeros((h.shape[0], cfg.H))
+    for t in range(h.shape[0]):
+        z = np.zeros(cfg.L)
+        hq = quant(h[t])
+        for k in range(cfg.K):
+            w1, w3, w2 = deq[int(idx[t, k])]
+            g, u = w1 @ hq, w3 @ hq
+            a = g / (1.0 + np.exp(-g)) * u
+            z += w[t, k] * (w2 @ quant(a))
+        n = z / np.sqrt(np.mean(z * z) + cfg.rms_eps) * gamma
+        out[t] = up @ n
+    return out
+
+
+def _rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def test_mxfp8_activations_exceed_the_parity_bar():
+    cfg = synth.SMALL_ALIGNED.with_tokens(16)
+    dense = synth.gen_dense(cfg)
+    x = synth.gen_x(cfg)
+    idx, _, _, _ = oracle.route(cfg, dense, x)
+    experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+    ref = oracle.forward(cfg, dense, experts, x, want_latent=True)
+    exact = _layer_from_latent(cfg, dense, experts, ref["h"], ref["idx"], ref["w"], lambda v: v)
+    # the re-statement reproduces the oracle (a second, independent reading of the steps)
+    assert _rel_l2(exact, ref["out"]) < 1e-12
+    # MXFP8 rounding of the two activation inputs alone costs several percent,
+    # above the 2e-2 rel-L2 bar, under either block-scale rule; the
+    # implementation therefore runs A16
+    for no_clip in (False, True):
+        q = lambda v: mxfp8(v, no_clip)
+        a8 = _layer_from_latent(cfg, dense, experts, ref["h"], ref["idx"], ref["w"], q)
+        err = _rel_l2(a8, ref["out"])
+        assert 2e-2 < err < 1e-1, (no_clip, err)
+        print(f"MXFP8 activations ({'no-clip' if no_clip else 'OCP'} scale): rel-L2 {err:.4f}")
