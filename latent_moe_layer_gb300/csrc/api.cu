@@ -359,7 +359,7 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
     }
     {
         k3_stage sg(h, K3MOE_STAGE_TOPK, st);
-        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
+        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, ws.counts, st))) return rc;
     }
     {
         k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);

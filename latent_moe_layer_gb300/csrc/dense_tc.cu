@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
                                                             const __grid_constant__ CUtensorMap bmap1,
                                                             const DenseArgs args)
 {
+    griddep_enter();
     using SM = DenseSmem<BN, NS>;
     constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
 __global__ void dense_reduce_kernel(const float *__restrict__ part, int splits, int M, int ldp, int c0, int n,
                                    float *__restrict__ out32, uint16_t *__restrict__ out16, int ldo)
 {
+    griddep_enter();
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (size_t)M * n) return;
     const int m = (int)(i / n), j = (int)(i % n);
@@ -255,7 +257,7 @@ static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUten
     int grid = 0;
     for (int s = 0; s < args.nseg; ++s) grid += args.seg[s].n_tiles * mt * args.seg[s].splits;
     if (grid == 0) return K3MOE_OK;
-    kern<<<grid, 192, SM::BYTES, st>>>(a, b0, b1, args);
+    k3_launch(kern, grid, 192, SM::BYTES, st, a, b0, b1, args);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
@@ -273,7 +275,7 @@ int k3_launch_dense_reduce(const float *part, int splits, int M, int ldp, int c0
 {
     const size_t total = (size_t)M * n;
     if (total == 0) return K3MOE_OK;
-    dense_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(part, splits, M, ldp, c0, n, out32, out16,
+    k3_launch(dense_reduce_kernel, (unsigned)((total + 255) / 256), 256, 0, st, part, splits, M, ldp, c0, n, out32, out16,
                                                                          ldo);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;

@@ -86,6 +86,7 @@ template <int NMAT, int NS, int MODE>
 __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_constant__ CUtensorMap bmap,
                                                              const GemvArgs a)
 {
+    griddep_enter();
     using SM = GvSmem<NMAT, NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -300,7 +301,7 @@ static int launch_gemv(const CUtensorMap &bmap, const GemvArgs &args, int max_it
         attr = true;
     }
     const int grid = max(1, min(max_items, 2 * num_sms));
-    kern<<<grid, 288, SM::BYTES, st>>>(bmap, args);
+    k3_launch(kern, grid, 288, SM::BYTES, st, bmap, args);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(256) rows_gemm_kernel(const void *__restrict__
                                                         float *__restrict__ out32,
                                                         uint16_t *__restrict__ out16, int accumulate)
 {
+    griddep_enter();
     __shared__ __align__(16) float sA[RG_TM][RG_KC];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m0 = blockIdx.y * RG_TM;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(256) glu_generic_kernel(
     const uint8_t *const *__restrict__ w3p, const uint8_t *const *__restrict__ w3s,
     const int32_t *__restrict__ offsets, int dint, float *__restrict__ act)
 {
+    griddep_enter();
     const int g = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int i = blockIdx.x * 8 + warp;
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(256) down_generic_kernel(
     const uint8_t *const *__restrict__ w2s, const int32_t *__restrict__ offsets, int dout,
     float *__restrict__ y, int accumulate)
 {
+    griddep_enter();
     const int g = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int o = blockIdx.x * 8 + warp;
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(
     const float *__restrict__ wts, const uint16_t *__restrict__ gamma, int K, int L, float eps,
     uint16_t *__restrict__ nrm)
 {
+    griddep_enter();
     const int t = blockIdx.x, tid = threadIdx.x;
     __shared__ float red[8];
     __shared__ int rows[64];
@@ -285,6 +289,7 @@ __global__ void __launch_bounds__(1024) combine_norm_v8_kernel(
     const uint16_t *__restrict__ y, const int32_t *__restrict__ row_of, const float *__restrict__ wts,
     const uint16_t *__restrict__ gamma, int K, int L, float eps, uint16_t *__restrict__ nrm)
 {
+    griddep_enter();
     const int t = blockIdx.x, tid = threadIdx.x;
     __shared__ float red[32];
     __shared__ int rows[64];
@@ -335,6 +340,7 @@ __global__ void __launch_bounds__(1024) combine_norm_v8_kernel(
 
 __global__ void finish_kernel(const float *__restrict__ o32, size_t n, uint16_t *__restrict__ out)
 {
+    griddep_enter();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) out[i] = f32_to_bf16(o32[i]);
 }
@@ -380,10 +386,10 @@ int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, 
     if (M == 0) return K3MOE_OK;
     dim3 grid((N + RG_ROWS - 1) / RG_ROWS, (M + RG_TM - 1) / RG_TM);
     if (grid.y > 65535) return K3MOE_ERR_UNSUPPORTED;
-    if (a_bf16 && w_bf16) rows_gemm_kernel<true, true><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
-    else if (a_bf16) rows_gemm_kernel<true, false><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
-    else if (w_bf16) rows_gemm_kernel<false, true><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
-    else rows_gemm_kernel<false, false><<<grid, 256, 0, st>>>(A, M, K, W, N, out_f32, out_bf16, accumulate);
+    if (a_bf16 && w_bf16) k3_launch(rows_gemm_kernel<true, true>, grid, 256, 0, st, A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else if (a_bf16) k3_launch(rows_gemm_kernel<true, false>, grid, 256, 0, st, A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else if (w_bf16) k3_launch(rows_gemm_kernel<false, true>, grid, 256, 0, st, A, M, K, W, N, out_f32, out_bf16, accumulate);
+    else k3_launch(rows_gemm_kernel<false, false>, grid, 256, 0, st, A, M, K, W, N, out_f32, out_bf16, accumulate);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }
@@ -397,7 +403,7 @@ int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token,
     (void)status;
     if (n_groups > 65535) return K3MOE_ERR_UNSUPPORTED;
     dim3 grid((dint + 7) / 8, n_groups);
-    glu_generic_kernel<<<grid, 256, 0, st>>>(in, din, row_token, rows, w1p, w1s, w3p, w3s, offsets, dint, act);
+    k3_launch(glu_generic_kernel, grid, 256, 0, st, in, din, row_token, rows, w1p, w1s, w3p, w3s, offsets, dint, act);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }
@@ -408,7 +414,7 @@ int k3_launch_down_generic(const float *act, int dint, int rows, const uint8_t *
 {
     if (n_groups > 65535) return K3MOE_ERR_UNSUPPORTED;
     dim3 grid((dout + 7) / 8, n_groups);
-    down_generic_kernel<<<grid, 256, 0, st>>>(act, dint, rows, w2p, w2s, offsets, dout, y, accumulate);
+    k3_launch(down_generic_kernel, grid, 256, 0, st, act, dint, rows, w2p, w2s, offsets, dout, y, accumulate);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }
@@ -421,11 +427,11 @@ int k3_launch_combine_norm(const void *y, int y_bf16, const int32_t *row_of, con
     if (L > 256 * CN_MAXV || K > 64) return K3MOE_ERR_UNSUPPORTED;
     if (y_bf16 && L % 8 == 0 && L / 8 <= 1024) {
         const int threads = ((L / 8) + 31) / 32 * 32;
-        combine_norm_v8_kernel<<<T, threads, 0, st>>>((const uint16_t *)y, row_of, wts, gamma, K, L, eps, nrm);
+        k3_launch(combine_norm_v8_kernel, T, threads, 0, st, (const uint16_t *)y, row_of, wts, gamma, K, L, eps, nrm);
         k3_note_launch();
         return K3_LAUNCH_OK();
     }
-    combine_norm_kernel<<<T, 256, 0, st>>>(y, y_bf16, row_of, wts, gamma, K, L, eps, nrm);
+    k3_launch(combine_norm_kernel, T, 256, 0, st, y, y_bf16, row_of, wts, gamma, K, L, eps, nrm);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }
@@ -433,7 +439,7 @@ int k3_launch_combine_norm(const void *y, int y_bf16, const int32_t *row_of, con
 int k3_launch_finish(const float *o32, int n, uint16_t *out, cudaStream_t st)
 {
     if (n == 0) return K3MOE_OK;
-    finish_kernel<<<(unsigned)(((size_t)n + 255) / 256), 256, 0, st>>>(o32, (size_t)n, out);
+    k3_launch(finish_kernel, (unsigned)(((size_t)n + 255) / 256), 256, 0, st, o32, (size_t)n, out);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }

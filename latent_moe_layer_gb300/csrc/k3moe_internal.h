@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "k3moe.h"
 
 #define K3_CUDA_TRY(expr)                                   \
@@ -62,6 +64,37 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code, float scale)
 // Kernel-launch counter (per host thread), read around each forward stage.
 extern thread_local long g_k3_launches;
 inline void k3_note_launch(int n = 1) { g_k3_launches += n; }
+
+// Forward-path launches use programmatic dependent launch: a kernel may be
+// scheduled while the previous kernel of the stream drains, and every such
+// kernel begins with griddep_wait() (all threads) before it reads anything
+// the previous kernels wrote, then lets its own dependent start launching.
+template <typename... KArgs, typename... Args>
+inline cudaError_t k3_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Wait until the previous kernel in the stream has completed and its writes are
+// visible, then allow the next kernel to be scheduled.
+__device__ __forceinline__ void griddep_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 // Stage timing ring (k3moe_profile_enable / k3moe_profile_read).
 struct k3_prof {
@@ -162,8 +195,8 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base 
 // --------------------------------------------------------------- launchers
 // routing and permutation (route.cu)
 int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
-                   cudaStream_t st);
-int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);
+                   int32_t *counts_zero, cudaStream_t st);   // counts_zero: [E] set to 0, or NULL
+int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);   // after top-k zeroed ws.counts
 
 // generic CUDA-core kernels (generic.cu)
 int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,

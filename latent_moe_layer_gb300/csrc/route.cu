@@ -21,8 +21,12 @@ template <int MAXP>
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits,
                                                    const float *__restrict__ bias, int T, int E,
                                                    int K, float scaling, int32_t *__restrict__ idx,
-                                                   float *__restrict__ wts)
+                                                   float *__restrict__ wts, int32_t *__restrict__ counts_zero)
 {
+    griddep_enter();
+    // the permutation's expert histogram starts from zero (the next kernel counts into it)
+    if (counts_zero && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < E; i += blockDim.x) counts_zero[i] = 0;
     __shared__ float skey[8][MAXP][32];
     const int wl = threadIdx.x >> 5;
     const int warp = blockIdx.x * 8 + wl;
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 __global__ void perm_count_kernel(const int32_t *__restrict__ idx, int n, int E,
                                   int32_t *__restrict__ counts, int *status)
 {
+    griddep_enter();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     int e = idx[i];
@@ -123,6 +128,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restri
                                                          int4 *__restrict__ tiles,
                                                          int32_t *__restrict__ meta)
 {
+    griddep_enter();
     __shared__ int s_cnt[1024], s_act[1024], s_til[1024];
     __shared__ int base_rows, base_act, base_til;
     const int tid = threadIdx.x;
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ tok_of,
                                                            int32_t *__restrict__ row_of)
 {
+    griddep_enter();
     const int e = blockIdx.x;
     if (counts[e] == 0) return;
     __shared__ int warp_tot[8];
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(256) perm_chunk_count_kernel(const int32_t *__
                                                                int E, int nch, int32_t *__restrict__ chunk_cnt,
                                                                int32_t *__restrict__ counts, int *status)
 {
+    griddep_enter();
     extern __shared__ int cnt[];                     // [E]
     const int ch = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -243,6 +251,7 @@ __global__ void __launch_bounds__(256) perm_chunk_count_kernel(const int32_t *__
 __global__ void __launch_bounds__(1024) perm_chunk_base_kernel(int nch, const int32_t *__restrict__ offsets,
                                                                int32_t *__restrict__ chunk_cnt)
 {
+    griddep_enter();
     __shared__ int s[1024];
     __shared__ int carry;
     const int e = blockIdx.x, tid = threadIdx.x;
@@ -274,6 +283,7 @@ __global__ void __launch_bounds__(32) perm_chunk_scatter_kernel(const int32_t *_
                                                                 int32_t *__restrict__ tok_of,
                                                                 int32_t *__restrict__ row_of)
 {
+    griddep_enter();
     extern __shared__ int next[];                    // [E] next free row per expert
     const int ch = blockIdx.x, lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) next[e] = chunk_base[(size_t)e * nch + ch];
@@ -299,16 +309,16 @@ __global__ void __launch_bounds__(32) perm_chunk_scatter_kernel(const int32_t *_
 using namespace k3;
 
 int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
-                   cudaStream_t st)
+                   int32_t *counts_zero, cudaStream_t st)
 {
     const k3moe_config &c = h->cfg;
     const float *bias = c.has_select_bias ? h->bias : nullptr;
     dim3 grid((T + 7) / 8), block(256);
     int E = c.n_experts;
-    if (E <= 128) topk_kernel<4><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
-    else if (E <= 256) topk_kernel<8><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
-    else if (E <= 512) topk_kernel<16><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
-    else if (E <= 1024) topk_kernel<32><<<grid, block, 0, st>>>(logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts);
+    if (E <= 128) k3_launch(topk_kernel<4>, grid, block, 0, st, logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts, counts_zero);
+    else if (E <= 256) k3_launch(topk_kernel<8>, grid, block, 0, st, logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts, counts_zero);
+    else if (E <= 512) k3_launch(topk_kernel<16>, grid, block, 0, st, logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts, counts_zero);
+    else if (E <= 1024) k3_launch(topk_kernel<32>, grid, block, 0, st, logits, bias, T, E, c.top_k, c.routed_scaling, idx, wts, counts_zero);
     else return K3MOE_ERR_UNSUPPORTED;
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
@@ -317,27 +327,27 @@ int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *i
 int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)
 {
     const int E = h->cfg.n_experts, K = h->cfg.top_k, n = T * K;
-    K3_CUDA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int32_t) * E, st));
+    // ws.counts was zeroed by the top-k kernel
     const bool chunked = T >= K3_PERM_CHUNKED_T;
     const int nch = (T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK;
     const size_t esm = sizeof(int) * E;              // E <= 1024: 4 KB of shared memory
     if (chunked) {
-        perm_chunk_count_kernel<<<nch, 256, esm, st>>>(ws.idx, T, K, E, nch, ws.chunk_cnt, ws.counts,
+        k3_launch(perm_chunk_count_kernel, nch, 256, esm, st, ws.idx, T, K, E, nch, ws.chunk_cnt, ws.counts,
                                                        h->d_status);
     } else {
-        perm_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(ws.idx, n, E, ws.counts, h->d_status);
+        k3_launch(perm_count_kernel, (n + 255) / 256, 256, 0, st, ws.idx, n, E, ws.counts, h->d_status);
     }
     k3_note_launch();
-    perm_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, E, tile_n, ws.offsets, ws.active,
+    k3_launch(perm_scan_kernel, 1, 1024, 0, st, ws.counts, E, tile_n, ws.offsets, ws.active,
                                          reinterpret_cast<int4 *>(ws.tiles), ws.meta);
     k3_note_launch();
     if (chunked) {
-        perm_chunk_base_kernel<<<E, 1024, 0, st>>>(nch, ws.offsets, ws.chunk_cnt);
+        k3_launch(perm_chunk_base_kernel, E, 1024, 0, st, nch, ws.offsets, ws.chunk_cnt);
         k3_note_launch();
-        perm_chunk_scatter_kernel<<<nch, 32, esm, st>>>(ws.idx, T, K, E, nch, ws.chunk_cnt, ws.tok_of,
+        k3_launch(perm_chunk_scatter_kernel, nch, 32, esm, st, ws.idx, T, K, E, nch, ws.chunk_cnt, ws.tok_of,
                                                         ws.row_of);
     } else {
-        perm_scatter_kernel<<<E, 256, 0, st>>>(ws.idx, n, K, ws.counts, ws.offsets, ws.tok_of, ws.row_of);
+        k3_launch(perm_scatter_kernel, E, 256, 0, st, ws.idx, n, K, ws.counts, ws.offsets, ws.tok_of, ws.row_of);
     }
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;

@@ -63,5 +63,5 @@ extern "C" int k3moe_route_static(k3moe_handle *h, const void *x, int T, int32_t
     rc = k3_launch_rows_gemm(x, 1, T, c.hidden, h->w_router, c.router_dtype == K3MOE_ROUTER_BF16,
                              c.n_experts, logits, nullptr, 0, stream);
     if (rc) return rc;
-    return k3_launch_topk(h, logits, T, idx_out, w_out, stream);
+    return k3_launch_topk(h, logits, T, idx_out, w_out, nullptr, stream);
 }

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
                                                            __half *__restrict__ dst,
                                                            float *__restrict__ rscale)
 {
+    griddep_enter();
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint16_t *s = src + (size_t)t * cols;
     float amax = 0.f;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
 // Token tiles of a dense (all-token) GEMM: (0, row0, rows) with at most bn rows.
 __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
 {
+    griddep_enter();
     const int n = (T + bn - 1) / bn;
     for (int i = threadIdx.x; i < n; i += blockDim.x) tiles[i] = make_int4(0, i * bn, min(bn, T - i * bn), 0);
     if (threadIdx.x == 0) *count = n;
@@ -155,7 +157,7 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
         attr = true;
     }
     const int grid = max(1, min(num_sms, max_tiles));
-    kern<<<grid, ex_threads(NMAT), SM::BYTES, st>>>(bmap, a);
+    k3_launch(kern, grid, ex_threads(NMAT), SM::BYTES, st, bmap, a);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
@@ -376,7 +378,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     if ((rc = dense_router_down(h, x, T, ws, st))) return rc;
     {
         k3_stage sg(h, K3MOE_STAGE_TOPK, st);
-        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, st))) return rc;
+        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, ws.counts, st))) return rc;
     }
     const bool gemv = bn == 32;     // routed experts at decode sizes: the streaming GEMV
     {   // token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
@@ -385,7 +387,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
-        prep_f16_rows_kernel<<<T, 256, 0, st>>>(ws.h, L, ws.row_of, K, (__half *)ws.hperm, ws.hscale);
+        k3_launch(prep_f16_rows_kernel, T, 256, 0, st, ws.h, L, ws.row_of, K, (__half *)ws.hperm, ws.hscale);
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
@@ -477,10 +479,10 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
         {
             k3_stage sg(h, K3MOE_STAGE_PREP, st);
-            prep_f16_rows_kernel<<<T, 256, 0, st>>>((const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
+            k3_launch(prep_f16_rows_kernel, T, 256, 0, st, (const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
                                                     ws.xscale);
             k3_note_launch();
-            dense_tiles_kernel<<<1, 256, 0, st>>>(T, sbn, stiles, ws.meta + 2);
+            k3_launch(dense_tiles_kernel, 1, 256, 0, st, T, sbn, stiles, ws.meta + 2);
             k3_note_launch();
             K3_CUDA_TRY(cudaGetLastError());
         }

@@ -121,6 +121,7 @@ template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
 __global__ void __launch_bounds__(ex_threads(NMAT), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
+    griddep_enter();
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
     constexpr int DQW = 4, NEPI = EX_NEPI;
     constexpr int EPI_WARP0 = 4 + DQW * NMAT;
