@@ -320,10 +320,10 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->hscale = cv.take<float>(R + 1);
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
     ws->o32 = cv.take<float>(Tn * c.hidden);
-    {   // split-K partials for the decode-size dense GEMMs: up to 8 splits
+    {   // split-K partials for the decode-size dense GEMMs: up to K3_DENSE_MAX_SPLITS splits
         const size_t ep = (size_t)((c.n_experts + 15) & ~15);
         const size_t w = ep + c.latent > (size_t)c.hidden ? ep + c.latent : (size_t)c.hidden;
-        ws->part_floats = T <= 256 ? (size_t)8 * Tn * w : 1;
+        ws->part_floats = T <= 256 ? (size_t)K3_DENSE_MAX_SPLITS * Tn * w : 1;
         ws->part = cv.take<float>(ws->part_floats);
     }
     ws->sact = cv.take<float>(c.shared_inter ? Tn * c.shared_inter : 1);

@@ -188,6 +188,8 @@ struct k3_ws {
 // Token permutation: from K3_PERM_CHUNKED_T tokens on, a chunked stable scatter
 // (tokens in chunks of K3_PERM_CHUNK) replaces the one-CTA-per-expert scan.
 constexpr int K3_PERM_CHUNK = 32;
+// Largest split-K factor of the decode-size dense GEMMs (partials buffer sizing).
+constexpr int K3_DENSE_MAX_SPLITS = 16;
 constexpr int K3_PERM_CHUNKED_T = 512;
 
 int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base may be NULL (sizing)

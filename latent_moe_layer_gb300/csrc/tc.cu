@@ -220,23 +220,33 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
     return K3MOE_OK;
 }
 
-// Smallest split-K factor (<= 8, dividing the K steps) giving at least `target` CTAs.
-static int choose_splits(int ksteps, int tiles, int target)
+// Split-K factor (dividing the K steps, <= K3_DENSE_MAX_SPLITS) whose CTAs each
+// stream close to `per_cta` K steps: every CTA of a launch then moves about the
+// same weight bytes, whichever segment it belongs to.
+static int choose_splits(int ksteps, double per_cta)
 {
     int best = 1;
-    for (int sp = 1; sp <= 8; ++sp) {
+    double err = 1e30;
+    for (int sp = 1; sp <= K3_DENSE_MAX_SPLITS; ++sp) {
         if (ksteps % sp) continue;
-        best = sp;
-        if (tiles * sp >= target) return sp;
+        const double e = fabs((double)ksteps / sp - per_cta);
+        if (e < err) {
+            err = e;
+            best = sp;
+        }
     }
     return best;
 }
+
+// K steps per CTA that spreads `tile_ksteps` (tiles x K steps, summed over the
+// launch's segments) over about two CTAs per SM.
+static double ksteps_per_cta(double tile_ksteps, int num_sms) { return tile_ksteps / (2.0 * num_sms); }
 
 // Decode-size token counts use BN = 128 tiles and split-K into fp32 partials
 // (two CTAs per SM); larger counts use BN = 256 tiles writing outputs directly.
 static bool dense_small(const k3_ws &ws, int T, size_t width)
 {
-    return T <= 256 && ws.part_floats >= (size_t)8 * T * width;
+    return T <= 256 && ws.part_floats >= (size_t)K3_DENSE_MAX_SPLITS * T * width;
 }
 
 // Router logits (fp32) and the latent h (BF16) in one tcgen05 launch.
@@ -268,11 +278,11 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     d.K = H;
     d.a_kmod = H;
     if (small) {
-        // split the work so both segments stream about the same bytes per CTA
-        const int target = 2 * h->num_sms;
-        const double wr = (double)r.K * E, wd = (double)d.K * L;
-        r.splits = choose_splits(r.K / 64, r.n_tiles * mt, (int)(target * wr / (wr + wd)));
-        d.splits = choose_splits(d.K / 64, d.n_tiles * mt, (int)(target * wd / (wr + wd)));
+        // split both segments so every CTA streams about the same weight bytes
+        const double per = ksteps_per_cta((double)mt * (r.n_tiles * (r.K / 64) + d.n_tiles * (d.K / 64)),
+                                          h->num_sms);
+        r.splits = choose_splits(r.K / 64, per);
+        d.splits = choose_splits(d.K / 64, per);
         // partial columns: router [0, Ep), down [Ep, Ep + L); Ep rounds E to 16 floats
         r.mode = d.mode = DN_OUT_F32;
         r.out = d.out = ws.part;
@@ -327,7 +337,7 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.mode = (!small && out16) ? DN_OUT_BF16 : DN_OUT_F32;
     u.col0 = 0;
     u.ldo = H;
-    u.splits = small ? choose_splits(L / 64, u.n_tiles * mt, 2 * h->num_sms) : 1;
+    u.splits = small ? choose_splits(L / 64, ksteps_per_cta((double)mt * u.n_tiles * (L / 64), h->num_sms)) : 1;
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
     int rc = k3_launch_dense_tc(bn, an, bu, bu, a, st);
     if (rc) return rc;
