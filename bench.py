@@ -339,6 +339,28 @@ def run_ours(args):
                "sample": f"{n} tokens of {cfg.name} (fp64 oracle, all layer steps), repeated to "
                          f"{nt} tokens in {dt:.2f} s"}
 
+    # Quantile-Balancing bias update (the training-time estimator of the
+    # selection bias), on seeded N(0, 1.5^2) router logits of this workload's shape
+    qb_line = None
+    if cfg.select_bias:
+        g = torch.Generator(device="cuda").manual_seed(7)
+        lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda") * 1.5
+        b0 = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            layer.qb_bias(lg, b0)
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        q0.record()
+        for _ in range(20):
+            layer.qb_bias(lg, b0)
+        q1.record()
+        torch.cuda.synchronize()
+        qms = q0.elapsed_time(q1) / 20
+        qbytes = 2 * cfg.T * cfg.E * 4                 # the logits are read twice
+        qb_line = {"ms": round(qms, 4), "algorithmic_bytes": qbytes,
+                   "achieved_gbs": round(qbytes / (qms / 1e3) / 1e9, 1),
+                   "frac": round(qbytes / (qms / 1e3) / 1e9 / pk["hbm_gbs"], 4), "nbins": 1000}
+
     exp_ms = stage_ms["gate_up"] + stage_ms["expert_down"]
     detail = {
         "stage_ms_per_step": {k: round(v / max(1, nfw), 4) for k, v in stage_ms.items() if v > 0},
@@ -349,6 +371,8 @@ def run_ours(args):
         "layer_tflops": round(sum(v[1] for v in work.values()) / (ms_step / 1e3) / 1e12, 3),
         "path": "tensor" if path_tensor else "generic",
     }
+    if qb_line:
+        detail["qb_bias_update"] = qb_line
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),

@@ -197,6 +197,34 @@ int k3moe_path_for(const k3moe_handle *h, int T);
 int k3moe_route_static(k3moe_handle *h, const void *x, int T, int32_t *idx_out, float *w_out,
                        cudaStream_t stream);
 
+/* ------------------------------------------------------------ QB bias update
+ * Quantile-Balancing selection-bias update ("the K3 report review", section on
+ * Quantile Balancing): the bias each expert should carry at the next step so
+ * that about q = T * top_k / n_experts of this batch's tokens select it.  It
+ * uses only the handle's configuration (n_experts, top_k); weights need not be
+ * loaded.
+ *
+ *   s[t][j]  = sigmoid(logits[t][j])
+ *   alpha[t] = the (top_k + 1)-th largest of s[t][j] + bias_in[j]
+ *   m[t][j]  = alpha[t] - s[t][j]   (token t selects j exactly when bias_j > m[t][j])
+ *   r        = round(T * top_k / n_experts), kept in [1, T - 1]
+ *   bias_out[j] = upper edge of the bin, among nbins equal bins spanning the
+ *                 batch's smallest to largest margin, that holds expert j's
+ *                 r-th smallest margin: within one bin width above that margin.
+ *
+ * logits:   device, fp32 [T, n_experts] row-major (the router's logits)
+ * bias_in:  device, fp32 [n_experts], or NULL for zeros (the current bias)
+ * bias_out: device, fp32 [n_experts]; may equal bias_in
+ * nbins:    1 .. 8192 (the source uses 1000)
+ * workspace: caller-owned device memory of k3moe_qb_workspace_bytes(h, T, nbins).
+ * Asynchronous on `stream`; the result depends only on the inputs (integer
+ * histogram counts).  Errors: K3MOE_ERR_ARG (NULL pointers, T < 2,
+ * nbins out of range), K3MOE_ERR_UNSUPPORTED (top_k + 1 > n_experts),
+ * K3MOE_ERR_WORKSPACE, K3MOE_ERR_CUDA. */
+size_t k3moe_qb_workspace_bytes(const k3moe_handle *h, int T, int nbins);
+int k3moe_qb_bias(k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
+                  int nbins, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------ profiling
  * Stage timing with CUDA events recorded on the launching stream around each
  * stage of k3moe_forward (a ring of 256 forwards), plus a count of kernel

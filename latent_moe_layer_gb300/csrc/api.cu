@@ -502,3 +502,21 @@ int k3moe_debug_wait_timeout(k3moe_handle *h, int spin_limit, cudaStream_t st)
 }
 
 }  // extern "C"
+
+extern "C" size_t k3moe_qb_workspace_bytes(const k3moe_handle *h, int T, int nbins)
+{
+    if (!h || T < 2 || nbins < 1 || nbins > 8192) return 0;
+    return k3_qb_workspace_bytes(T, h->cfg.n_experts, nbins);
+}
+
+extern "C" int k3moe_qb_bias(k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
+                             int nbins, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!h || !logits || !bias_out || !workspace) return K3MOE_ERR_ARG;
+    if (T < 2 || nbins < 1 || nbins > 8192) return K3MOE_ERR_ARG;
+    if (h->cfg.top_k + 1 > h->cfg.n_experts) return K3MOE_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (dev != h->device) return K3MOE_ERR_STATE;
+    return k3_qb_bias(h, logits, T, bias_in, bias_out, nbins, workspace, workspace_bytes, stream);
+}

@@ -198,6 +198,9 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base 
 // routing and permutation (route.cu)
 int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
                    int32_t *counts_zero, cudaStream_t st);   // counts_zero: [E] set to 0, or NULL
+size_t k3_qb_workspace_bytes(int T, int E, int nbins);
+int k3_qb_bias(const k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
+               int nbins, void *ws, size_t ws_bytes, cudaStream_t st);
 int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);   // after top-k zeroed ws.counts
 
 // generic CUDA-core kernels (generic.cu)

@@ -24,7 +24,8 @@ ROUTER_F32, ROUTER_BF16 = 0, 1
 EXPORTS = ["k3moe_create", "k3moe_persistent_bytes", "k3moe_load_weights", "k3moe_workspace_bytes",
            "k3moe_forward", "k3moe_forward_host", "k3moe_status", "k3moe_destroy", "k3moe_strerror",
            "k3moe_path_for", "k3moe_debug_dequant", "k3moe_debug_wait_timeout",
-           "k3moe_profile_enable", "k3moe_profile_read", "k3moe_stage_name"]
+           "k3moe_profile_enable", "k3moe_profile_read", "k3moe_stage_name", "k3moe_qb_workspace_bytes",
+           "k3moe_qb_bias"]
 STAGES = ["router", "down_proj", "topk", "permute", "gate_up", "expert_down", "combine_norm",
           "up_proj", "shared", "finish", "prep"]
 
@@ -86,6 +87,9 @@ def lib():
         L.k3moe_profile_read.argtypes = [vp, vp, vp, vp]
         L.k3moe_stage_name.argtypes = [i]
         L.k3moe_stage_name.restype = C.c_char_p
+        L.k3moe_qb_workspace_bytes.argtypes = [vp, i, i]
+        L.k3moe_qb_workspace_bytes.restype = sz
+        L.k3moe_qb_bias.argtypes = [vp, vp, i, vp, vp, i, vp, sz, vp]
         for name in EXPORTS:
             getattr(L, name)
         _lib = L
@@ -205,6 +209,19 @@ class Layer:
         if rc < 0:
             check(rc, "profile_read")
         return rc, {STAGES[i]: ms[i] for i in range(n)}, {STAGES[i]: la[i] for i in range(n)}
+
+    def qb_bias(self, logits, bias_in=None, nbins=1000, stream=None):
+        """Quantile-Balancing bias update from router logits (fp32 CUDA [T, E]) -> fp32 [E]."""
+        import torch
+        T = logits.shape[0]
+        n = lib().k3moe_qb_workspace_bytes(self.h, T, nbins)
+        if n == 0:
+            raise K3Error(ERR_CODE["ARG"], "qb_workspace_bytes")
+        ws = torch.empty(n, dtype=torch.uint8, device=logits.device)
+        out = torch.empty(logits.shape[1], dtype=torch.float32, device=logits.device)
+        check(lib().k3moe_qb_bias(self.h, logits.data_ptr(), T, _ptr(bias_in), out.data_ptr(), nbins,
+                                  ws.data_ptr(), n, _stream_ptr(stream)), "qb_bias")
+        return out
 
     def debug_wait_timeout(self, spin_limit, stream=None):
         check(lib().k3moe_debug_wait_timeout(self.h, spin_limit, _stream_ptr(stream)), "wait")
