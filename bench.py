@@ -71,7 +71,11 @@ def stage_work(cfg, touched, path_tensor):
     w["expert_down"] = (touched * mx(L, I) + R * I * act_b + R * L * act_b, 2 * R * L * I)
     w["combine_norm"] = (R * L * act_b + T * L * 2, 0)
     w["up_proj"] = (H * L * 2 + T * L * 2 + T * H * 4, 2 * T * H * L)
-    w["shared"] = ((2 * mx(S, H) + mx(H, S) + T * H * 2 + T * H * 4) if S else 0, 6 * T * S * H)
+    if path_tensor:
+        w["shared"] = ((2 * mx(S, H) + T * H * 2 + T * S * 2) if S else 0, 4 * T * S * H)
+        w["shared_down"] = ((mx(H, S) + T * S * 2 + T * H * 8) if S else 0, 2 * T * H * S)
+    else:
+        w["shared"] = ((2 * mx(S, H) + mx(H, S) + T * H * 2 + T * H * 4) if S else 0, 6 * T * S * H)
     w["finish"] = (T * H * 6, 0)
     w["prep"] = (R * L * 4, 0)
     return w

@@ -237,10 +237,11 @@ int k3moe_qb_bias(k3moe_handle *h, const float *logits, int T, const float *bias
 #define K3MOE_STAGE_EXPERT_DOWN 5   /* expert w2 */
 #define K3MOE_STAGE_COMBINE     6   /* combine + RMSNorm */
 #define K3MOE_STAGE_UP          7   /* routed_expert_up_proj */
-#define K3MOE_STAGE_SHARED      8   /* shared experts */
+#define K3MOE_STAGE_SHARED      8   /* shared experts: gate/up + activation (the whole GLU on the generic path) */
 #define K3MOE_STAGE_FINISH      9   /* output conversion */
 #define K3MOE_STAGE_PREP       10   /* activation conversion for the tensor path */
-#define K3MOE_NUM_STAGES       11
+#define K3MOE_STAGE_SHARED_DOWN 11  /* shared experts: down projection (tensor path) */
+#define K3MOE_NUM_STAGES       12
 
 int k3moe_profile_enable(k3moe_handle *h, int enable);
 /* Synchronise `stream`, then write per-stage milliseconds summed over the

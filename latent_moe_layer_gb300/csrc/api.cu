@@ -191,7 +191,7 @@ const char *k3moe_stage_name(int s)
 {
     static const char *names[K3MOE_NUM_STAGES] = {"router", "down_proj", "topk", "permute", "gate_up",
                                                   "expert_down", "combine_norm", "up_proj", "shared",
-                                                  "finish", "prep"};
+                                                  "finish", "prep", "shared_down"};
     return (s >= 0 && s < K3MOE_NUM_STAGES) ? names[s] : "?";
 }
 

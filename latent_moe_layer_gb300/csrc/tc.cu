@@ -522,7 +522,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         s2.out = ws.o32;
         const int nt = (T + sbn - 1) / sbn;
         if ((rc = expert_pair(h, sbn, sb1, sb2, s1, s2, nt * (S / EX_BM), nt * (H / EX_BM), st,
-                              K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED, true)))
+                              K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED_DOWN, true)))
             return rc;
     }
     k3_stage sg(h, K3MOE_STAGE_FINISH, st);

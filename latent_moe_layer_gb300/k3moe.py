@@ -27,7 +27,7 @@ EXPORTS = ["k3moe_create", "k3moe_persistent_bytes", "k3moe_load_weights", "k3mo
            "k3moe_profile_enable", "k3moe_profile_read", "k3moe_stage_name", "k3moe_qb_workspace_bytes",
            "k3moe_qb_bias"]
 STAGES = ["router", "down_proj", "topk", "permute", "gate_up", "expert_down", "combine_norm",
-          "up_proj", "shared", "finish", "prep"]
+          "up_proj", "shared", "finish", "prep", "shared_down"]
 
 
 class K3Error(RuntimeError):
