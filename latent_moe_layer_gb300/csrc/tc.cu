@@ -355,7 +355,7 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 // activation slots.
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
-                       cudaStream_t st, int stage1, int stage2, bool f32_add)
+                       cudaStream_t st, int stage1, int stage2, bool add)
 {
     int rc;
     const int ns = h->num_sms;
@@ -368,9 +368,9 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
     {
         k3_stage sg(h, stage2, st);
         // the tile list was cut at bn rows: the kernel's BN must equal bn
-        if (f32_add)
-            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st)
-                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_F32_ADD>(b2, a2, max_tiles2, ns, st);
+        if (add)
+            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16_ADD>(b2, a2, max_tiles2, ns, st)
+                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16_ADD>(b2, a2, max_tiles2, ns, st);
         else
             rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
                           : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
@@ -519,12 +519,12 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         s2.rows = H;
         s2.K = S;
         s2.rscale = nullptr;
-        s2.out = ws.o32;
+        s2.addend = ws.o32;                          // the up-projection's fp32 output
+        s2.out = out;                                // BF16 layer output = up + shared, rounded once
         const int nt = (T + sbn - 1) / sbn;
         if ((rc = expert_pair(h, sbn, sb1, sb2, s1, s2, nt * (S / EX_BM), nt * (H / EX_BM), st,
                               K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED_DOWN, true)))
             return rc;
     }
-    k3_stage sg(h, K3MOE_STAGE_FINISH, st);
-    return k3_launch_finish(ws.o32, T * H, (uint16_t *)out, st);
+    return K3MOE_OK;
 }

@@ -32,7 +32,7 @@
 
 namespace k3 {
 
-enum ExpertOut { OUT_GLU_F16 = 0, OUT_BF16 = 1, OUT_F32_ADD = 2 };
+enum ExpertOut { OUT_GLU_F16 = 0, OUT_BF16 = 1, OUT_BF16_ADD = 2 };
 
 struct ExpertGemmArgs {
     const CUtensorMap *amaps;        // global: maps of group g, matrix m at amaps[g * amap_stride + amap_off[m]]
@@ -45,7 +45,8 @@ struct ExpertGemmArgs {
     const int4 *tiles;               // (group, row0, nrows, -) per token tile
     const int *n_tiles;              // device count of tiles
     const float *rscale;             // per B-row factor (GLU input scaling) or nullptr
-    void *out;                       // GLU: f16 [R, rows]; BF16: [R, rows]; F32_ADD: fp32 [R, rows]
+    void *out;                       // GLU: f16 [R, rows]; BF16 and BF16_ADD: BF16 [R, rows]
+    const float *addend;             // BF16_ADD: fp32 [R, rows] added before the rounding to BF16
     int *status;
     uint32_t spin_limit;
 };
@@ -423,6 +424,18 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
             const int nchunks = (nrows + 15) >> 4;
             for (int c = half; c < nchunks; c += NEPI / 4) {
+                // BF16_ADD: the chunk's addends are read before the TMEM loads, so
+                // their latency overlaps them
+                float ad0[16], ad1[16];
+                if (MODE == OUT_BF16_ADD) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c * 16 + j;
+                        const float *ar = args.addend + (size_t)(row0 + (n < nrows ? n : 0)) * args.rows;
+                        ad0[j] = ar[row];
+                        ad1[j] = ROWPAIR ? ar[row1] : 0.f;
+                    }
+                }
                 uint32_t v0[16], v1[16];
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
@@ -445,9 +458,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                             o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
                             if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * fw1);
                         } else {
-                            float *o = reinterpret_cast<float *>(args.out) + orow * args.rows;
-                            o[row] += __uint_as_float(v0[j]) * fw0;
-                            if (ROWPAIR) o[row1] += __uint_as_float(v1[j]) * fw1;
+                            uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
+                            o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * fw0);
+                            if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * fw1);
                         }
                     }
                 }
