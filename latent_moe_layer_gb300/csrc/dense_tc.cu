@@ -25,8 +25,11 @@ struct DenseSmem {
     static constexpr int B_BYTES = BN * DN_BK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int OFF_BAR = NS * STAGE;
-    static constexpr int BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
+    static constexpr int N_BAR = 2 * NS + 4 + 1;          // full/empty per stage, tfull/tempty x 2, drain
+    static constexpr int BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;
 };
+
+constexpr int DN_THREADS = 320;    // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two per TMEM lane quarter)
 
 __device__ __forceinline__ bool dn_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
                                         int where)
@@ -43,47 +46,67 @@ __device__ __forceinline__ bool dn_wait(uint32_t bar, uint32_t parity, volatile 
     return false;
 }
 
+struct DnTile {
+    int seg, split, n0, m0, k0, ks;
+};
+
+// segment by value (a select between the two parameter copies, no indexed access)
+__device__ __forceinline__ DenseSeg dn_seg(const DenseArgs &args, int seg) { return seg ? args.seg[1] : args.seg[0]; }
+
+// tile index -> (segment, split, n tile, m tile); segment 0's tiles come first
+__device__ __forceinline__ DnTile dn_tile(const DenseArgs &args, int t, int mt_n, int BN)
+{
+    DnTile r;
+    const int per0 = args.seg[0].n_tiles * mt_n * args.seg[0].splits;
+    r.seg = 0;
+    if (t >= per0) {
+        r.seg = 1;
+        t -= per0;
+    }
+    const DenseSeg S = dn_seg(args, r.seg);
+    r.split = t % S.splits;
+    t /= S.splits;
+    r.m0 = (t % mt_n) * DN_BM;
+    r.n0 = (t / mt_n) * BN;
+    r.ks = S.K / DN_BK / S.splits;
+    r.k0 = r.split * r.ks;
+    return r;
+}
+
+// Persistent over the output tiles: the TMA ring runs across tile boundaries,
+// and two TMEM accumulator sets let the epilogue of one tile overlap the
+// MMAs of the next.
 template <int BN, int NS>
-__global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
-                                                            const __grid_constant__ CUtensorMap bmap0,
-                                                            const __grid_constant__ CUtensorMap bmap1,
-                                                            const DenseArgs args)
+__global__ void __launch_bounds__(DN_THREADS, 2) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                 const __grid_constant__ CUtensorMap bmap0,
+                                                                 const __grid_constant__ CUtensorMap bmap1,
+                                                                 const DenseArgs args)
 {
     griddep_enter();
     using SM = DenseSmem<BN, NS>;
-    constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    constexpr uint32_t TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+    static_assert(2 * BN <= 512, "two accumulator sets");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = (uint64_t *)(smem + SM::OFF_BAR), *empty = full + NS, *done = empty + NS;
-    uint32_t *tmem_holder = (uint32_t *)(done + 1);
+    uint64_t *full = (uint64_t *)(smem + SM::OFF_BAR), *empty = full + NS;
+    uint64_t *tfull = empty + NS, *tempty = tfull + 2, *drain = tempty + 2;
+    uint32_t *tmem_holder = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // tile -> (segment, n tile, m tile, split)
-    int tid = blockIdx.x;
     const int mt_n = (args.M + DN_BM - 1) / DN_BM;
-    int seg = 0;
-    const int per0 = args.seg[0].n_tiles * mt_n * args.seg[0].splits;
-    if (tid >= per0) {
-        seg = 1;
-        tid -= per0;
-    }
-    const DenseSeg &S = args.seg[seg];
-    const int split = tid % S.splits;
-    tid /= S.splits;
-    const int mt = tid % mt_n;
-    const int nt = tid / mt_n;
-    const int n0 = nt * BN, m0 = mt * DN_BM;
-    const int ks_per = S.K / DN_BK / S.splits;
-    const int k0 = split * ks_per;
-    const CUtensorMap *bm = seg == 0 ? &bmap0 : &bmap1;
+    const int total = args.seg[0].n_tiles * mt_n * args.seg[0].splits +
+                      (args.nseg > 1 ? args.seg[1].n_tiles * mt_n * args.seg[1].splits : 0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(full + i), 1);
             mbar_init(smem_u32(empty + i), 1);
         }
-        mbar_init(smem_u32(done), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(tfull + i), 1);
+            mbar_init(smem_u32(tempty + i), 8);
+        }
+        mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -99,56 +122,89 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
         prefetch_tmap(&amap);
-        prefetch_tmap(bm);
+        prefetch_tmap(&bmap0);
+        if (args.nseg > 1) prefetch_tmap(&bmap1);
         const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-        int issued = 0;
-        for (int s = 0; s < ks_per; ++s, ++issued) {
-            const int slot = s % NS;
-            if (!dn_wait(smem_u32(empty + slot), ((s / NS) & 1) ^ 1, abort_flag, args.status, 21)) break;
-            const uint32_t fb = smem_u32(full + slot);
-            mbar_expect_tx(fb, SM::STAGE);
-            uint8_t *st = smem + slot * SM::STAGE;
-            const int k = (k0 + s) * DN_BK;
-            tma_load_2d_hint(smem_u32(st), &amap, fb, k % S.a_kmod, m0, pol_a);
-            tma_load_2d_hint(smem_u32(st + SM::A_BYTES), bm, fb, k, n0, pol_w);
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+            const DnTile d = dn_tile(args, t, mt_n, BN);
+            const DenseSeg S = dn_seg(args, d.seg);
+            const CUtensorMap *bm = d.seg == 0 ? &bmap0 : &bmap1;
+            bool ok = true;
+            for (int s = 0; s < d.ks; ++s, ++it) {
+                const int slot = it % NS;
+                if (!dn_wait(smem_u32(empty + slot), ((it / NS) & 1) ^ 1, abort_flag, args.status, 21)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(full + slot);
+                mbar_expect_tx(fb, SM::STAGE);
+                uint8_t *st = smem + slot * SM::STAGE;
+                const int k = (d.k0 + s) * DN_BK;
+                tma_load_2d_hint(smem_u32(st), &amap, fb, k % S.a_kmod, d.m0, pol_a);
+                tma_load_2d_hint(smem_u32(st + SM::A_BYTES), bm, fb, k, d.n0, pol_w);
+            }
+            if (!ok) break;
         }
-        const int n = issued < NS ? issued : NS;
-        for (int q = 0; q < n; ++q) {
-            const int i2 = issued - 1 - q;
+        const uint32_t n = it < (uint32_t)NS ? it : (uint32_t)NS;
+        for (uint32_t q = 0; q < n; ++q) {
+            const uint32_t i2 = it - 1 - q;
             mbar_wait(smem_u32(full + i2 % NS), (i2 / NS) & 1, 0xFFFFFFFFu);
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc = idesc_f16(DN_BM, BN, 1);
-        for (int s = 0; s < ks_per; ++s) {
-            const int slot = s % NS;
-            if (!dn_wait(smem_u32(full + slot), (s / NS) & 1, abort_flag, args.status, 22)) break;
+        uint32_t it = 0, tc = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+            const DnTile d = dn_tile(args, t, mt_n, BN);
+            const int acc = (int)(tc & 1);
+            if (!dn_wait(smem_u32(tempty + acc), ((tc >> 1) & 1) ^ 1, abort_flag, args.status, 24)) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + slot * SM::STAGE);
-            const uint64_t adesc = smem_desc_sw128(a_addr), bdesc = smem_desc_sw128(a_addr + SM::A_BYTES);
+            const uint32_t dcol = tmem + acc * BN;
+            bool ok = true;
+            for (int s = 0; s < d.ks; ++s, ++it) {
+                const int slot = it % NS;
+                if (!dn_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, args.status, 22)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + slot * SM::STAGE);
+                const uint64_t adesc = smem_desc_sw128(a_addr), bdesc = smem_desc_sw128(a_addr + SM::A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < DN_BK / 16; ++kk)
-                tc_mma_f16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(empty + slot));
+                for (int kk = 0; kk < DN_BK / 16; ++kk)
+                    tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(smem_u32(empty + slot));
+            }
+            if (!ok) break;
+            tc_commit(smem_u32(tfull + acc));
         }
-        tc_commit(smem_u32(done));
+        // every issued MMA completes before TMEM is released
+        tc_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, 0xFFFFFFFFu);
     } else if (warp >= 2) {
-        // ------------------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------------------ epilogue (warps 2..9)
         const int q = warp & 3;                       // TMEM lanes 32q .. 32q + 31
-        const int m = m0 + 32 * q + lane;
-        const bool ok = dn_wait(smem_u32(done), 0, abort_flag, args.status, 23);
-        tc_fence_after();
-        if (ok) {
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
-            for (int c = 0; c < BN / 16; ++c) {
+        const int half = (warp - 2) >> 2;             // chunks c with c % 2 == half
+        uint32_t tc = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+            const DnTile d = dn_tile(args, t, mt_n, BN);
+            const DenseSeg S = dn_seg(args, d.seg);
+            const int acc = (int)(tc & 1);
+            const int m = d.m0 + 32 * q + lane;
+            if (!dn_wait(smem_u32(tfull + acc), (tc >> 1) & 1, abort_flag, args.status, 23)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * BN;
+            for (int c = half; c < BN / 16; c += 2) {
                 uint32_t v[16];
                 tmem_ld16(tbase + c * 16, v);
                 tc_wait_ld();
-                const int n = n0 + 16 * c;
+                const int n = d.n0 + 16 * c;
                 const int nv = S.n_out - n;                 // valid columns in this chunk
                 if (m < args.M && nv > 0) {
                     if (S.mode == DN_OUT_F32) {
-                        float *o = reinterpret_cast<float *>(S.out) + ((size_t)split * args.M + m) * S.ldo + S.col0 + n;
+                        float *o = reinterpret_cast<float *>(S.out) + ((size_t)d.split * args.M + m) * S.ldo +
+                                   S.col0 + n;
                         if (nv >= 16 && ((uintptr_t)o & 15) == 0) {
 #pragma unroll
                             for (int j = 0; j < 16; j += 4)
@@ -178,6 +234,9 @@ __global__ void __launch_bounds__(192) dense_gemm_kernel(const __grid_constant__
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
         }
     }
     tc_fence_before();
@@ -242,7 +301,7 @@ bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, i
 
 template <int BN, int NS>
 static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const DenseArgs &args,
-                        cudaStream_t st)
+                        int num_sms, cudaStream_t st)
 {
     using SM = DenseSmem<BN, NS>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
@@ -254,19 +313,22 @@ static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUten
         attr = true;
     }
     const int mt = (args.M + DN_BM - 1) / DN_BM;
-    int grid = 0;
-    for (int s = 0; s < args.nseg; ++s) grid += args.seg[s].n_tiles * mt * args.seg[s].splits;
-    if (grid == 0) return K3MOE_OK;
-    k3_launch(kern, grid, 192, SM::BYTES, st, a, b0, b1, args);
+    int tiles = 0;
+    for (int s = 0; s < args.nseg; ++s) tiles += args.seg[s].n_tiles * mt * args.seg[s].splits;
+    if (tiles == 0) return K3MOE_OK;
+    // persistent: as many CTAs as fit on the GPU at once (shared memory bound)
+    const int per_sm = (228 * 1024) / (SM::BYTES + 1024) > 1 ? 2 : 1;
+    const int grid = std::min(tiles, per_sm * num_sms);
+    k3_launch(kern, grid, DN_THREADS, SM::BYTES, st, a, b0, b1, args);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
 
 int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                       const DenseArgs &args, cudaStream_t st)
+                       const DenseArgs &args, int num_sms, cudaStream_t st)
 {
-    if (bn == 128) return launch_dense<128, 3>(a, b0, b1, args, st);   // 2 CTAs per SM (decode sizes)
-    if (bn == 256) return launch_dense<256, 4>(a, b0, b1, args, st);
+    if (bn == 128) return launch_dense<128, 3>(a, b0, b1, args, num_sms, st);   // 2 CTAs per SM (decode sizes)
+    if (bn == 256) return launch_dense<256, 4>(a, b0, b1, args, num_sms, st);
     return K3MOE_ERR_UNSUPPORTED;
 }
 

@@ -33,7 +33,7 @@ struct DenseArgs {
 // X rows [rows, cols] BF16 (or weights): box 64 x box_rows, 128-byte swizzle.
 bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
 int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                       const k3::DenseArgs &args, cudaStream_t st);
+                       const k3::DenseArgs &args, int num_sms, cudaStream_t st);
 // out = sum over splits of part[s][m][c0 + j], j < n (fp32 and/or BF16 outputs, row stride ldo).
 int k3_launch_dense_reduce(const float *part, int splits, int M, int ldp, int c0, int n, float *out32,
                            uint16_t *out16, int ldo, cudaStream_t st);

@@ -303,7 +303,7 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     int rc;
     {
         k3_stage sg(h, K3MOE_STAGE_ROUTER, st);
-        if ((rc = k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, st))) return rc;
+        if ((rc = k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, h->num_sms, st))) return rc;
     }
     if (small) {
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
@@ -339,7 +339,7 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.ldo = H;
     u.splits = small ? choose_splits(L / 64, ksteps_per_cta((double)mt * u.n_tiles * (L / 64), h->num_sms)) : 1;
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
-    int rc = k3_launch_dense_tc(bn, an, bu, bu, a, st);
+    int rc = k3_launch_dense_tc(bn, an, bu, bu, a, h->num_sms, st);
     if (rc) return rc;
     if (small)
         rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, out16 ? nullptr : ws.o32, out16, H, st);
