@@ -88,6 +88,18 @@ def test_wide_scale_exponents(path, T):
     assert_parity(compare(cfg, g, ref))
 
 
+# Token counts on each side of the tensor path's internal switches (SMALL_ALIGNED:
+# E = 24, K = 4): decode GEMV vs 256-row tcgen05 tiles at T K = 24 E (T = 144),
+# split-K dense GEMMs up to T = 256, the chunked permutation from T = 512.
+@pytest.mark.parametrize("T", [1, 144, 145, 256, 257, 511, 512])
+def test_tensor_path_switch_boundaries(T):
+    cfg = synth.SMALL_ALIGNED.with_tokens(T)
+    g = run_gpu(cfg, TEN)
+    assert g["status"] == 0 and g["path"] == TEN
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
 def test_tensor_and_generic_paths_agree():
     cfg = synth.SMALL_SHARED.with_tokens(64)
     a = run_gpu(cfg, GEN)
