@@ -271,12 +271,9 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                             const float av = gv / (1.0f + expf(-gv)) * uv;
                             if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
                             reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
-                        } else if (MODE == GV_BF16) {
+                        } else {
                             reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] =
                                 f32_to_bf16(acc[0][nb][q] * f0);
-                        } else {
-                            float *o = reinterpret_cast<float *>(a.out) + orow * a.rows + row;
-                            *o += acc[0][nb][q] * f0;
                         }
                     }
                 }
@@ -311,5 +308,5 @@ int k3_launch_gemv_expert(int glu, int mode, const CUtensorMap &bmap, const Gemv
 {
     if (glu) return launch_gemv<2, 2, GV_GLU_F16>(bmap, args, max_items, num_sms, st);
     if (mode == GV_BF16) return launch_gemv<1, 4, GV_BF16>(bmap, args, max_items, num_sms, st);
-    return launch_gemv<1, 4, GV_F32_ADD>(bmap, args, max_items, num_sms, st);
+    return K3MOE_ERR_UNSUPPORTED;
 }

@@ -6,7 +6,7 @@
 
 namespace k3 {
 
-enum GemvOut { GV_GLU_F16 = 0, GV_BF16 = 1, GV_F32_ADD = 2 };
+enum GemvOut { GV_GLU_F16 = 0, GV_BF16 = 1 };
 
 struct GemvArgs {
     const CUtensorMap *amaps;          // global: packed map of group g, matrix m at amaps[g * amap_stride + amap_off[m]]
@@ -18,7 +18,7 @@ struct GemvArgs {
     const int4 *tiles;                 // (group, first B row, B rows <= 16) per token tile
     const int *n_tiles;                // device count of tiles
     const float *rscale;               // [R] per-row factor applied to the GLU inputs, or nullptr
-    void *out;                         // GLU: f16 [R, rows]; BF16: [R, rows]; F32_ADD: fp32 [R, rows]
+    void *out;                         // GLU: f16 [R, rows]; BF16: BF16 [R, rows]
     int *status;
 };
 

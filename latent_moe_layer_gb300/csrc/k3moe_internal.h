@@ -171,7 +171,7 @@ struct k3_ws {
     void *hperm;          // [T*K, L] f16 (tensor path) activation rows in expert order
     float *hscale;        // [T*K] per-row power-of-two factor of hperm
     uint16_t *nrm;        // [T, L] BF16 normalised latent
-    float *o32;           // [T, H] fp32 up_proj (+ shared) accumulator
+    float *o32;           // [T, H] fp32 up_proj output (generic path: + shared; tensor path: the shared down's addend)
     float *part;          // split-K partials of the dense tensor-core GEMMs (small T only)
     size_t part_floats;
     void *sact;           // [T, S] shared-expert activation (fp32 generic / f16 tensor)
