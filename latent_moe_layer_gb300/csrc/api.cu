@@ -357,14 +357,7 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
         if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_down, 1, L, nullptr, ws.h, 0, st))) return rc;
     }
-    {
-        k3_stage sg(h, K3MOE_STAGE_TOPK, st);
-        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, ws.counts, st))) return rc;
-    }
-    {
-        k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
-        if ((rc = k3_launch_permute(h, ws, T, 0, st))) return rc;
-    }
+    if ((rc = k3_launch_route(h, ws, T, 0, st))) return rc;   // top-K and the permutation
     {
         k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
         if ((rc = k3_launch_glu_generic(ws.h, L, ws.tok_of, R, h->d_eptr[0], h->d_eptr[1], h->d_eptr[2],

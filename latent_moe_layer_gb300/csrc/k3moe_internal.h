@@ -202,6 +202,8 @@ size_t k3_qb_workspace_bytes(int T, int E, int nbins);
 int k3_qb_bias(const k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
                int nbins, void *ws, size_t ws_bytes, cudaStream_t st);
 int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);   // after top-k zeroed ws.counts
+// Top-K then the permutation (one fused launch at decode sizes), with their profiling stages.
+int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st);
 
 // generic CUDA-core kernels (generic.cu)
 int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,

@@ -11,29 +11,18 @@
 
 namespace k3 {
 
-// One warp per token (8 tokens per CTA).  Lane l owns keys j = l + 32 i (a
-// column of a [MAXP][32] tile in shared memory) and keeps the best untaken key
-// of its column.  Each of the K rounds takes the warp-wide maximum of the lane
-// bests (equal keys: lower index), marks it taken, and the warp rescans only the
+// Top-K of one token, one warp.  Lane l owns keys j = l + 32 i (a column of a
+// [MAXP][32] tile in shared memory) and keeps the best untaken key of its
+// column.  Each of the K rounds takes the warp-wide maximum of the lane bests
+// (equal keys: lower index), marks it taken, and the warp rescans only the
 // winning lane's column.  NaN keys rank below every number.  Writes idx in
-// selection order and the weights sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
+// selection order (and to sidx when given) and the weights
+// sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
 template <int MAXP>
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits,
-                                                   const float *__restrict__ bias, int T, int E,
-                                                   int K, float scaling, int32_t *__restrict__ idx,
-                                                   float *__restrict__ wts, int32_t *__restrict__ counts_zero)
+__device__ __forceinline__ void topk_warp(const float *__restrict__ lrow, const float *__restrict__ bias, int E,
+                                          int K, float scaling, float (*col)[32], int lane,
+                                          int32_t *__restrict__ idx_row, float *__restrict__ w_row, int *sidx)
 {
-    griddep_enter();
-    // the permutation's expert histogram starts from zero (the next kernel counts into it)
-    if (counts_zero && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < E; i += blockDim.x) counts_zero[i] = 0;
-    __shared__ float skey[8][MAXP][32];
-    const int wl = threadIdx.x >> 5;
-    const int warp = blockIdx.x * 8 + wl;
-    const int lane = threadIdx.x & 31;
-    if (warp >= T) return;
-    const float *lrow = logits + (size_t)warp * E;
-    float (*col)[32] = skey[wl];
     float bk = -INFINITY;
     int bj = 0x7fffffff;
 #pragma unroll
@@ -100,9 +89,30 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     if (lane < K) {
         const float l = lrow[sel_j];
         const float sg = 1.0f / (1.0f + expf(-l));
-        idx[(size_t)warp * K + lane] = sel_j;
-        wts[(size_t)warp * K + lane] = sg / ssum * scaling;
+        idx_row[lane] = sel_j;
+        w_row[lane] = sg / ssum * scaling;
+        if (sidx) sidx[lane] = sel_j;
     }
+}
+
+// One warp per token (8 tokens per CTA).
+template <int MAXP>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits,
+                                                   const float *__restrict__ bias, int T, int E,
+                                                   int K, float scaling, int32_t *__restrict__ idx,
+                                                   float *__restrict__ wts, int32_t *__restrict__ counts_zero)
+{
+    griddep_enter();
+    // the permutation's expert histogram starts from zero (the next kernel counts into it)
+    if (counts_zero && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < E; i += blockDim.x) counts_zero[i] = 0;
+    __shared__ float skey[8][MAXP][32];
+    const int wl = threadIdx.x >> 5;
+    const int warp = blockIdx.x * 8 + wl;
+    const int lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    topk_warp<MAXP>(logits + (size_t)warp * E, bias, E, K, scaling, skey[wl], lane, idx + (size_t)warp * K,
+                    wts + (size_t)warp * K, nullptr);
 }
 
 // counts[e] = number of (t, k) selecting e; flags an index outside [0, E).
@@ -120,15 +130,13 @@ __global__ void perm_count_kernel(const int32_t *__restrict__ idx, int n, int E,
     atomicAdd(counts + e, 1);
 }
 
-// Single CTA: offsets = exclusive scan of counts; active-expert list; tile list
-// for the tensor path (expert, first row, rows) with at most tile_n rows each.
-__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restrict__ counts, int E,
-                                                         int tile_n, int32_t *__restrict__ offsets,
-                                                         int32_t *__restrict__ active,
-                                                         int4 *__restrict__ tiles,
-                                                         int32_t *__restrict__ meta)
+// One CTA of 1024 threads: offsets = exclusive scan of counts; active-expert
+// list; tile list for the tensor path (expert, first row, rows) with at most
+// tile_n rows each.  Ends with the CTA synchronised and its writes visible to it.
+__device__ __forceinline__ void perm_scan_block(const int32_t *counts, int E, int tile_n,
+                                                int32_t *__restrict__ offsets, int32_t *__restrict__ active,
+                                                int4 *__restrict__ tiles, int32_t *__restrict__ meta)
 {
-    griddep_enter();
     __shared__ int s_cnt[1024], s_act[1024], s_til[1024];
     __shared__ int base_rows, base_act, base_til;
     const int tid = threadIdx.x;
@@ -174,6 +182,58 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restri
         offsets[E] = base_rows;
         meta[0] = base_act;
         meta[1] = base_til;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restrict__ counts, int E,
+                                                         int tile_n, int32_t *__restrict__ offsets,
+                                                         int32_t *__restrict__ active,
+                                                         int4 *__restrict__ tiles,
+                                                         int32_t *__restrict__ meta)
+{
+    griddep_enter();
+    perm_scan_block(counts, E, tile_n, offsets, active, tiles, meta);
+}
+
+// Decode-size routing in one CTA (T <= 32 tokens, T K <= 1024 pairs, E <= 1024):
+// top-K per token (warp t), the expert histogram in shared memory, the scan and
+// tile list, and the stable scatter (a pair's row within its expert is the
+// number of earlier pairs, in (t, k) order, that chose the same expert).
+template <int MAXP>
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int K, float scaling,
+    int32_t *__restrict__ idx, float *__restrict__ wts, int tile_n, int32_t *__restrict__ offsets,
+    int32_t *__restrict__ active, int4 *__restrict__ tiles, int32_t *__restrict__ meta,
+    int32_t *__restrict__ tok_of, int32_t *__restrict__ row_of, int *status)
+{
+    griddep_enter();
+    extern __shared__ float rs_keys[];                // [32][MAXP][32]
+    __shared__ int s_idx[1024], s_hist[1024];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, n = T * K;
+    s_hist[tid] = 0;
+    __syncthreads();
+    if (w < T)
+        topk_warp<MAXP>(logits + (size_t)w * E, bias, E, K, scaling,
+                        reinterpret_cast<float(*)[32]>(rs_keys + (size_t)w * MAXP * 32), lane, idx + (size_t)w * K,
+                        wts + (size_t)w * K, s_idx + w * K);
+    __syncthreads();
+    if (tid < n) {
+        const int e = s_idx[tid];
+        if (e < 0 || e >= E) set_status(status, K3MOE_ERR_RANGE, e);
+        else atomicAdd(&s_hist[e], 1);
+    }
+    __syncthreads();
+    perm_scan_block(s_hist, E, tile_n, offsets, active, tiles, meta);
+    if (tid < n) {
+        const int e = s_idx[tid];
+        if (e >= 0 && e < E) {
+            int rank = 0;
+            for (int q = 0; q < tid; ++q) rank += s_idx[q] == e;
+            const int row = offsets[e] + rank;
+            tok_of[row] = tid / K;
+            row_of[tid] = row;
+        }
     }
 }
 
@@ -322,6 +382,46 @@ int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *i
     else return K3MOE_ERR_UNSUPPORTED;
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+template <int MAXP>
+static int launch_route_small(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)
+{
+    const k3moe_config &c = h->cfg;
+    auto kern = route_small_kernel<MAXP>;
+    const size_t smem = sizeof(float) * 32 * MAXP * 32;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return K3MOE_ERR_CUDA;
+        attr = true;
+    }
+    const float *bias = c.has_select_bias ? h->bias : nullptr;
+    k3_launch(kern, 1, 1024, smem, st, ws.logits, bias, T, c.n_experts, c.top_k, c.routed_scaling, ws.idx, ws.wts,
+              tile_n, ws.offsets, ws.active, reinterpret_cast<int4 *>(ws.tiles), ws.meta, ws.tok_of, ws.row_of,
+              h->d_status);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)
+{
+    const int E = h->cfg.n_experts, K = h->cfg.top_k;
+    int rc;
+    if (T <= 32 && T * K <= 1024 && E <= 1024) {
+        // one launch for top-K and the permutation
+        k3_stage sg(h, K3MOE_STAGE_TOPK, st);
+        if (E <= 128) return launch_route_small<4>(h, ws, T, tile_n, st);
+        if (E <= 256) return launch_route_small<8>(h, ws, T, tile_n, st);
+        if (E <= 512) return launch_route_small<16>(h, ws, T, tile_n, st);
+        return launch_route_small<32>(h, ws, T, tile_n, st);
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_TOPK, st);
+        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, ws.counts, st))) return rc;
+    }
+    k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
+    return k3_launch_permute(h, ws, T, tile_n, st);
 }
 
 int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)

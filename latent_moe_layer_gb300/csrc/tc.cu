@@ -386,15 +386,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     const int bn = pick_bn(T, K, E);
     int rc;
     if ((rc = dense_router_down(h, x, T, ws, st))) return rc;
-    {
-        k3_stage sg(h, K3MOE_STAGE_TOPK, st);
-        if ((rc = k3_launch_topk(h, ws.logits, T, ws.idx, ws.wts, ws.counts, st))) return rc;
-    }
     const bool gemv = bn == 32;     // routed experts at decode sizes: the streaming GEMV
-    {   // token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
-        k3_stage sg(h, K3MOE_STAGE_PERMUTE, st);
-        if ((rc = k3_launch_permute(h, ws, T, gemv ? 16 : bn, st))) return rc;
-    }
+    // top-K and the permutation; token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
+    if ((rc = k3_launch_route(h, ws, T, gemv ? 16 : bn, st))) return rc;
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
         k3_launch(prep_f16_rows_kernel, T, 256, 0, st, ws.h, L, ws.row_of, K, (__half *)ws.hperm, ws.hscale);
