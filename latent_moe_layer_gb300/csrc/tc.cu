@@ -144,12 +144,12 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
     if (threadIdx.x == 0) *count = n;
 }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
 int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
-    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
-    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE>;
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE, ATMEM>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
@@ -163,7 +163,17 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
 }
 
 // Tile shape by the token count per expert: small N for decode batches.
-int pick_bn(int T, int K, int E) { return ((size_t)T * K <= (size_t)E * 24) ? 32 : 256; }
+// Tile shape by rows per expert: decode batches (<= 24 on average) take the
+// GEMV; up to 192 on average (partly filled tiles) take 192-token tiles with the
+// decoded weights in TMEM, which keeps shared memory below its bandwidth limit;
+// more take 256-token tiles, which amortise the dequantisation and the epilogue
+// over more tokens.
+int pick_bn(int T, int K, int E)
+{
+    const size_t R = (size_t)T * K;
+    if (R <= (size_t)E * 24) return 32;
+    return R <= (size_t)E * 192 ? 192 : 256;
+}
 
 }  // namespace
 
@@ -348,11 +358,12 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
 // accumulator sets NACC).  N <= 32 (shared experts at small T): gate/up 3/4/2/2
-// (176 KB smem), down 4/4/4/2 (144 KB).  N <= 256: both 2/3/2/1
-// (224 KB; 512 TMEM columns), the down projection taking 256 weight rows per job
-// (two 128-row blocks against one activation tile, halving activation traffic).
-// Activation loads are latency-bound, so the spare shared memory goes to
-// activation slots.
+// (176 KB smem), down 4/4/4/2 (144 KB).  N <= 192: both 3/5/2/1 with the A slots
+// in TMEM (2 x 192 accumulator + 2 x 2 x 32 A columns = 512; 216 KB smem).
+// N <= 256: both 2/3/2/1 (224 KB; 512 TMEM columns).  The down projection takes
+// 256 weight rows per job (two 128-row blocks against one activation tile,
+// halving activation traffic).  Activation loads are latency-bound, so spare
+// shared memory goes to activation slots.
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool add)
@@ -361,19 +372,22 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
     const int ns = h->num_sms;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32 ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
-                      : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
+        rc = bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
+             : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true>(b1, a1, max_tiles1, ns, st)
+                         : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
         // the tile list was cut at bn rows: the kernel's BN must equal bn
+        // shared-expert down projections (add) always run at 256 tokens or at 32
         if (add)
             rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16_ADD>(b2, a2, max_tiles2, ns, st)
                           : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16_ADD>(b2, a2, max_tiles2, ns, st);
         else
-            rc = bn == 32 ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
-                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
+            rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
+                 : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_BF16, true>(b2, a2, max_tiles2, ns, st)
+                             : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
 }

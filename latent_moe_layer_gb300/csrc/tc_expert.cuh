@@ -64,13 +64,13 @@ struct ActMaps {
     CUtensorMap big, small;
 };
 
-template <int NMAT, int BN, int NS, int NB, int NA>
+template <int NMAT, int BN, int NS, int NB, int NA, bool ATMEM = false>
 struct ExpertSmem {
     static constexpr int PK_BYTES = EX_BM * EX_KP / 2;      // 16384 packed bytes per matrix
     static constexpr int B_BYTES = BN * EX_KS * 2;          // activation sub-tile
     static constexpr int A_BYTES = EX_BM * EX_KS * 2;       // 16384 f16 tile
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + NA * NMAT * A_BYTES;
+    static constexpr int OFF_B = OFF_A + (ATMEM ? 0 : NA * NMAT * A_BYTES);   // ATMEM: A lives in TMEM
     static constexpr int OFF_PK = OFF_B + NB * B_BYTES;
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
     static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
@@ -118,15 +118,18 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
 constexpr int EX_NEPI = 8;
 __host__ __device__ constexpr int ex_threads(int nmat) { return (4 + 4 * nmat + EX_NEPI) * 32; }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
 __global__ void __launch_bounds__(ex_threads(NMAT), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
     griddep_enter();
-    using SM = ExpertSmem<NMAT, BN, NS, NB, NA>;
+    using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
     constexpr int DQW = 4, NEPI = EX_NEPI;
     constexpr int EPI_WARP0 = 4 + DQW * NMAT;
-    constexpr int COLS = NACC * NMAT * BN;       // NACC accumulator sets (2: epilogue overlaps the next tile)
+    // TMEM columns: NACC accumulator sets (2: the epilogue overlaps the next tile),
+    // then with ATMEM the NA x NMAT decoded A sub-tiles (128 lanes x 32 columns each)
+    constexpr int ACOL0 = NACC * NMAT * BN;
+    constexpr int COLS = ACOL0 + (ATMEM ? NA * NMAT * EX_KS / 2 : 0);
     constexpr uint32_t TMEM_COLS = (COLS <= 32) ? 32 : (COLS <= 64) ? 64 : (COLS <= 128) ? 128
                                  : (COLS <= 256) ? 256 : 512;
     static_assert(COLS <= 512 && (NACC == 1 || NACC == 2), "TMEM columns");
@@ -274,12 +277,20 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + SM::OFF_B + bslot * SM::B_BYTES));
 #pragma unroll
                     for (int mt = 0; mt < NMAT; ++mt) {
-                        const uint64_t adesc =
-                            smem_desc_sw128(smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES));
+                        if (ATMEM) {
+                            const uint32_t acol = tmem + ACOL0 + (aslot * NMAT + mt) * (EX_KS / 2);
 #pragma unroll
-                        for (int kk = 0; kk < EX_KS / 16; ++kk)
-                            tc_mma_f16(dcol + mt * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                       (ks > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < EX_KS / 16; ++kk)   // 16 K = 8 columns
+                                tc_mma_f16_ts(dcol + mt * BN, acol + 8 * kk, bdesc + 2 * kk, idesc,
+                                              (ks > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t adesc =
+                                smem_desc_sw128(smem_u32(smem + SM::OFF_A + (aslot * NMAT + mt) * SM::A_BYTES));
+#pragma unroll
+                            for (int kk = 0; kk < EX_KS / 16; ++kk)
+                                tc_mma_f16(dcol + mt * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                           (ks > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit(smem_u32(bempty + bslot));
                     tc_commit(smem_u32(aempty + aslot));
@@ -362,6 +373,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                     uint8_t *arow = smem + SM::OFF_A + (aslot * NMAT + mat) * SM::A_BYTES + r * 128;
                     const uint4 lo = c[2 * q], hi = c[2 * q + 1];
                     const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    uint32_t tv[ATMEM ? 32 : 1];                 // ATMEM: the row's 64 values in K order
+                    if (ATMEM) tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         uint32_t h0, h1, h2, h3;
@@ -380,9 +393,26 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         v.y = *reinterpret_cast<uint32_t *>(&q1);
                         v.z = *reinterpret_cast<uint32_t *>(&q2);
                         v.w = *reinterpret_cast<uint32_t *>(&q3);
-                        *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
+                        if (ATMEM) {
+                            tv[(4 * j + 0) % (ATMEM ? 32 : 1)] = v.x;
+                            tv[(4 * j + 1) % (ATMEM ? 32 : 1)] = v.y;
+                            tv[(4 * j + 2) % (ATMEM ? 32 : 1)] = v.z;
+                            tv[(4 * j + 3) % (ATMEM ? 32 : 1)] = v.w;
+                        } else {
+                            *reinterpret_cast<uint4 *>(arow + 16 * (j ^ (r & 7))) = v;
+                        }
                     }
-                    fence_proxy_async_smem();
+                    if (ATMEM) {
+                        // lanes 32 (warp % 4) .. +31 = rows r of this warp; columns of A slot (aslot, mat)
+                        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + ACOL0 +
+                                            (aslot * NMAT + mat) * (EX_KS / 2);
+                        tmem_st16(ta, tv);
+                        tmem_st16(ta + 16, tv + (ATMEM ? 16 : 0));
+                        tc_wait_st();
+                        tc_fence_before();
+                    } else {
+                        fence_proxy_async_smem();
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(afull + aslot));
                 }
