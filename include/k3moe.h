@@ -127,12 +127,16 @@ size_t k3moe_persistent_bytes(const k3moe_handle *h);
 int k3moe_load_weights(k3moe_handle *h, const k3moe_weights *w, void *persistent,
                        size_t persistent_bytes, cudaStream_t stream);
 
+/* Largest T accepted by the per-call entry points (T * top_k stays far inside
+ * int range); larger T returns K3MOE_ERR_ARG (workspace_bytes returns 0). */
+#define K3MOE_MAX_TOKENS (1 << 24)
+
 /* Bytes of per-call device workspace for T tokens (256-byte aligned base),
  * including the staging used by k3moe_forward_host. */
 size_t k3moe_workspace_bytes(const k3moe_handle *h, int T);
 
 /*
- * Forward T >= 0 tokens.  x: [T, H] BF16 device; out: [T, H] BF16 device (must
+ * Forward 0 <= T <= K3MOE_MAX_TOKENS tokens.  x: [T, H] BF16 device; out: [T, H] BF16 device (must
  * not overlap x: K3MOE_ERR_ALIAS).  idx_out [T, K] int32 and w_out [T, K] fp32
  * (optional, may be NULL) receive the selected experts in selection order and
  * their mixture weights.  T == 0 is a no-op.  Asynchronous on `stream`; the

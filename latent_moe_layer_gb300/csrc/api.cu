@@ -289,7 +289,7 @@ int k3moe_path_for(const k3moe_handle *h, int T)
 
 size_t k3moe_workspace_bytes(const k3moe_handle *h, int T)
 {
-    if (!h || T < 0) return 0;
+    if (!h || T < 0 || T > K3_MAX_TOKENS) return 0;
     k3_ws ws;
     k3_ws_layout(h, T, nullptr, &ws);
     return ws.bytes;
@@ -405,7 +405,7 @@ static int forward_impl(k3moe_handle *h, const void *x, int T, void *out, int32_
 {
     if (!h) return K3MOE_ERR_ARG;
     if (!h->loaded) return K3MOE_ERR_STATE;
-    if (T < 0) return K3MOE_ERR_ARG;
+    if (T < 0 || T > K3_MAX_TOKENS) return K3MOE_ERR_ARG;
     if (T == 0) return K3MOE_OK;
     if (!x || !out || !workspace) return K3MOE_ERR_ARG;
     const k3moe_config &c = h->cfg;
@@ -448,7 +448,7 @@ int k3moe_forward_host(k3moe_handle *h, const void *x_host, int T, void *out_hos
 {
     if (!h) return K3MOE_ERR_ARG;
     if (!h->loaded) return K3MOE_ERR_STATE;
-    if (T < 0) return K3MOE_ERR_ARG;
+    if (T < 0 || T > K3_MAX_TOKENS) return K3MOE_ERR_ARG;
     if (T == 0) return K3MOE_OK;
     if (!x_host || !out_host || !workspace) return K3MOE_ERR_ARG;
     if ((uintptr_t)workspace % 256) return K3MOE_ERR_ALIGN;

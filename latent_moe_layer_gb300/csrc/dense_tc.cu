@@ -306,12 +306,8 @@ static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUten
     using SM = DenseSmem<BN, NS>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
     auto kern = dense_gemm_kernel<BN, NS>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
-            return K3MOE_ERR_CUDA;
-        attr = true;
-    }
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int mt = (args.M + DN_BM - 1) / DN_BM;
     int tiles = 0;
     for (int s = 0; s < args.nseg; ++s) tiles += args.seg[s].n_tiles * mt * args.seg[s].splits;

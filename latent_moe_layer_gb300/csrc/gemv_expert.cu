@@ -291,12 +291,8 @@ static int launch_gemv(const CUtensorMap &bmap, const GemvArgs &args, int max_it
     using SM = GvSmem<NMAT, NS>;
     static_assert(2 * SM::BYTES <= 228 * 1024, "two CTAs per SM");
     auto kern = gemv_expert_kernel<NMAT, NS, MODE>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
-            return K3MOE_ERR_CUDA;
-        attr = true;
-    }
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int grid = max(1, min(max_items, 2 * num_sms));
     k3_launch(kern, grid, 288, SM::BYTES, st, bmap, args);
     k3_note_launch();

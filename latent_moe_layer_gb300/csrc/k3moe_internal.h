@@ -65,6 +65,23 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code, float scale)
 extern thread_local long g_k3_launches;
 inline void k3_note_launch(int n = 1) { g_k3_launches += n; }
 
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute is
+// per device; `done` is the launcher's own bitmask of devices already set).
+template <typename F>
+inline bool k3_smem_attr(F kern, int bytes, unsigned long long &done)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done & bit)) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done |= bit;
+    return true;
+}
+
+// Largest token count of one call (K3MOE_MAX_TOKENS of the public header).
+constexpr int K3_MAX_TOKENS = K3MOE_MAX_TOKENS;
+
 // Forward-path launches use programmatic dependent launch: a kernel may be
 // scheduled while the previous kernel of the stream drains, and every such
 // kernel begins with griddep_wait() (all threads) before it reads anything

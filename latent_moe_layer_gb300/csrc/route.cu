@@ -390,12 +390,8 @@ static int launch_route_small(const k3moe_handle *h, const k3_ws &ws, int T, int
     const k3moe_config &c = h->cfg;
     auto kern = route_small_kernel<MAXP>;
     const size_t smem = sizeof(float) * 32 * MAXP * 32;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return K3MOE_ERR_CUDA;
-        attr = true;
-    }
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, (int)smem, attr_set)) return K3MOE_ERR_CUDA;
     const float *bias = c.has_select_bias ? h->bias : nullptr;
     k3_launch(kern, 1, 1024, smem, st, ws.logits, bias, T, c.n_experts, c.top_k, c.routed_scaling, ws.idx, ws.wts,
               tile_n, ws.offsets, ws.active, reinterpret_cast<int4 *>(ws.tiles), ws.meta, ws.tok_of, ws.row_of,

@@ -46,7 +46,7 @@ extern "C" int k3moe_route_static(k3moe_handle *h, const void *x, int T, int32_t
 {
     if (!h) return K3MOE_ERR_ARG;
     if (!h->loaded) return K3MOE_ERR_STATE;
-    if (T < 0) return K3MOE_ERR_ARG;
+    if (T < 0 || T > K3_MAX_TOKENS) return K3MOE_ERR_ARG;
     if (T == 0) return K3MOE_OK;
     if (!x || !idx_out || !w_out) return K3MOE_ERR_ARG;
     if ((uintptr_t)x % 16) return K3MOE_ERR_ALIGN;

@@ -150,12 +150,8 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
     auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE, ATMEM>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES) != cudaSuccess)
-            return K3MOE_ERR_CUDA;
-        attr = true;
-    }
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int grid = max(1, min(num_sms, max_tiles));
     k3_launch(kern, grid, ex_threads(NMAT), SM::BYTES, st, bmap, a);
     k3_note_launch();

@@ -191,6 +191,11 @@ def test_errors_are_reported():
                            16, s) == k3moe.ERR_CODE["WORKSPACE"]
     assert L.k3moe_forward(layer.h, x.data_ptr(), -1, out.data_ptr(), None, None, ws.data_ptr(),
                            ws.numel(), s) == k3moe.ERR_CODE["ARG"]
+    # above the documented token limit
+    big = (1 << 24) + 1
+    assert L.k3moe_forward(layer.h, x.data_ptr(), big, out.data_ptr(), None, None, ws.data_ptr(),
+                           ws.numel(), s) == k3moe.ERR_CODE["ARG"]
+    assert L.k3moe_workspace_bytes(layer.h, big) == 0
     assert L.k3moe_forward(layer.h, x.data_ptr() + 2, cfg.T, out.data_ptr(), None, None,
                            ws.data_ptr(), ws.numel(), s) == k3moe.ERR_CODE["ALIGN"]
     assert layer.status() == 0
