@@ -74,7 +74,7 @@ def test_small_aligned_parity(path, name, T):
 
 
 @pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
-@pytest.mark.parametrize("T", [40, 300], ids=["decode_tiles", "tcgen05_tiles"])
+@pytest.mark.parametrize("T", [40, 300, 1500], ids=["decode_tiles", "tmem_a_192_tiles", "smem_a_256_tiles"])
 def test_wide_scale_exponents(path, T):
     # E8M0 exponents uniform over 96..126: a row's blocks sit up to 30 binary
     # orders below its largest, so the fast paths' exact f16 decode meets its
