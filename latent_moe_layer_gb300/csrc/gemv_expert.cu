@@ -1,23 +1,22 @@
 // Decode-batch expert kernels: streaming MXFP4 GEMV for experts with few tokens.
 //
 // When each touched expert sees only a handful of tokens the layer is bound by
-// reading the touched experts' packed bytes once from HBM.  These kernels
-// decode FP4 in registers straight from 64-bit coalesced global loads -- the
-// packed bytes never go through shared memory, and nothing is expanded there
-// -- and feed the warp-level tensor-core MMA (m16n8k16, f16 inputs, fp32
+// reading the touched experts' packed bytes once from HBM.  A TMA warp streams
+// the packed rows (and the tile's few activation rows) into a shared-memory
+// ring; consumer warps decode FP4 in registers (nothing is expanded in shared
+// memory) and feed the warp-level tensor-core MMA (m16n8k16, f16 inputs, fp32
 // accumulate) with the decoded weights as the A fragment and up to 16 token
-// rows as B.
+// rows as B.  Activation rows are the per-token power-of-two scaled f16 copies
+// prepared for the tensor path.
 //
-// Exactness: as in the tcgen05 path, row m's weights are decoded as
-// E2M1 x 2^(e - emax_m) in f16 (exact for e >= emax_m - 23) and 2^(emax_m - 127)
-// is applied to the fp32 result; activation rows are the per-token
-// power-of-two scaled f16 copies prepared for the tensor path.
-//
-// K order: for each 64-wide K step, thread (g = lane/4, c = lane%4) loads bytes
-// [8c, 8c+8) of rows g and g+8, i.e. 16 consecutive codes of one MX block, and
-// uses its pairs 2s and 2s+1 as MMA k-step s's pair slots c and c+4.  The B
-// fragment reads the matching activation elements (K = 16c + 4s .. +3), so the
-// contraction covers every K exactly once in a permuted order.
+// Block scales (OCP MX v1.0: value = E2M1 x 2^(e - 127), e the block's E8M0
+// byte): each MMA covers one MX block only.  Thread (g = lane/4, c = lane%4)
+// holds bytes [4c, 4c+4) of the block for weight rows g and g+8, i.e.
+// block-local K = 8c .. 8c+7, used as the k-steps {8c, 8c+1 | 8c+2, 8c+3} and
+// {8c+4, 8c+5 | 8c+6, 8c+7}; the B fragments read the activations at the same
+// K.  The MMAs run on the plain E2M1 values (exact in f16) and the block's fp32
+// partial sum is multiplied by 2^(e - 127) (exact in fp32; code 0 is taken as 0)
+// and added to the row's accumulator.
 #include "gemv_expert.h"
 #include "tc_expert.cuh"
 
@@ -25,53 +24,32 @@ namespace k3 {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint2 ldg_stream(const uint8_t *p)
+// 8 codes (one 32-bit word, low nibble first) -> 4 f16x2 of the plain E2M1 values.
+__device__ __forceinline__ void decode8(uint32_t w, uint32_t (&o)[4])
 {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
-// 8 codes (one 32-bit word, low nibble first) -> 4 f16x2 of E2M1 values times `sc`.
-__device__ __forceinline__ void decode8(uint32_t w, __half2 sc, uint32_t (&o)[4])
-{
-    uint32_t h0, h1, h2, h3;
     asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
         "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
         "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
         : "r"(w));
-    __half2 q0 = __hmul2(*reinterpret_cast<__half2 *>(&h0), sc);
-    __half2 q1 = __hmul2(*reinterpret_cast<__half2 *>(&h1), sc);
-    __half2 q2 = __hmul2(*reinterpret_cast<__half2 *>(&h2), sc);
-    __half2 q3 = __hmul2(*reinterpret_cast<__half2 *>(&h3), sc);
-    o[0] = *reinterpret_cast<uint32_t *>(&q0);
-    o[1] = *reinterpret_cast<uint32_t *>(&q1);
-    o[2] = *reinterpret_cast<uint32_t *>(&q2);
-    o[3] = *reinterpret_cast<uint32_t *>(&q3);
 }
 
-__device__ __forceinline__ __half2 pow2_h2(int d)
-{
-    // 2^d (d <= 0) as f16x2: built exactly in fp32 (d clamped at -126, far below
-    // f16's range) and rounded once to f16 -- subnormals below 2^-14, zero below 2^-24
-    const float f = __int_as_float((max(d, -126) + 127) << 23);
-    return __float2half2_rn(f);
-}
+// 2^(e - 127) for the E8M0 byte `e`, exact in fp32 (e = 0 is taken as 0).
+__device__ __forceinline__ float e8m0_f32_noden(uint32_t e) { return __uint_as_float(e << 23); }
 
 // Packed FP4 rows arrive by TMA (per-expert tensor maps: 128 rows x 128 bytes
 // = 256 K values per stage, 128-byte swizzle) into a ring of NS stages; eight
 // consumer warps, 16 weight rows each, read their bytes out of shared memory,
 // decode them in registers and run the MMAs.  Work items are (token tile of the
-// permutation, 128-row block); activation fragments come from global memory
-// (the few token rows of a tile stay in L1/L2).
+// permutation, 128-row block); each stage also carries the tile's activation
+// rows (16 rows x 256 K, four 64-K boxes), which stay L2-resident across the
+// row blocks of an expert.
 constexpr int GV_STAGE_BYTES = 128 * 128;    // one matrix, one stage
 constexpr int GV_B_BYTES = 4 * 16 * 128;     // 16 activation rows x 256 K (four 64-K boxes)
 
@@ -81,6 +59,91 @@ struct GvSmem {
     static constexpr int OFF_BAR = NS * STAGE;
     static constexpr int BYTES = OFF_BAR + 2 * NS * 8 + 16 + 1024;
 };
+
+// One work item's K loop for a tile of NNB x 8 token rows (the token count is a
+// template argument so that the unrolled loop carries no branches).
+template <int NMAT, int NS, int NNB>
+__device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t *full, uint64_t *empty,
+                                            volatile int *abort_flag, const GemvArgs &a, int nkp, int ra_l,
+                                            int g8, int c, int lane, const uint2 *const (&sa)[NMAT], int rbo,
+                                            uint32_t &it, float (&acc)[NMAT][2][4])
+{
+    using SM = GvSmem<NMAT, NS>;
+    const int rb_l = ra_l + 8;
+    // scale bytes: 8 per row and stage (blocks 8s .. 8s+7), read one stage ahead
+    uint2 sca[NMAT], scb[NMAT], nsa[NMAT], nsb[NMAT];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+        nsa[m] = __ldg(sa[m]);
+        nsb[m] = __ldg(sa[m] + rbo);
+    }
+    for (int s = 0; s < nkp; ++s, ++it) {
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            sca[m] = nsa[m];
+            scb[m] = nsb[m];
+            if (s + 1 < nkp) {
+                nsa[m] = __ldg(sa[m] + s + 1);
+                nsb[m] = __ldg(sa[m] + rbo + s + 1);
+            }
+        }
+        const int slot = it % NS;
+        if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, 0xFFFFFFFFu, a.status, 12)) return false;
+        const uint8_t *sbase = smem + slot * SM::STAGE;
+        const uint8_t *bbase = sbase + NMAT * GV_STAGE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+            for (int bl = 0; bl < 2; ++bl) {
+                // MX block j = 2 ks + bl of the stage = 16-byte chunk j of each 128-byte row;
+                // this thread takes bytes [4c, 4c + 4) of it
+                const int j = 2 * ks + bl;
+                uint32_t pa[NMAT], pb[NMAT];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const uint8_t *base = sbase + m * GV_STAGE_BYTES;
+                    pa[m] = *reinterpret_cast<const uint32_t *>(base + ra_l * 128 + 16 * (j ^ g8) + 4 * c);
+                    pb[m] = *reinterpret_cast<const uint32_t *>(base + rb_l * 128 + 16 * (j ^ g8) + 4 * c);
+                }
+                // token 8 nb + g8 at block-local K = 8c .. 8c + 7: 16-byte chunk 4 bl + c of its
+                // row in box ks (128-byte swizzle)
+                uint4 hb[NNB];
+#pragma unroll
+                for (int nb = 0; nb < NNB; ++nb)
+                    hb[nb] = *reinterpret_cast<const uint4 *>(bbase + ks * 16 * 128 + (8 * nb + g8) * 128 +
+                                                              16 * ((4 * bl + c) ^ g8));
+                if (ks == 3 && bl == 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(empty + slot));
+                }
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const uint32_t wsa = (j >> 2) ? sca[m].y : sca[m].x;
+                    const uint32_t wsb = (j >> 2) ? scb[m].y : scb[m].x;
+                    const float fa = e8m0_f32_noden((wsa >> (8 * (j & 3))) & 0xFFu);
+                    const float fb = e8m0_f32_noden((wsb >> (8 * (j & 3))) & 0xFFu);
+                    uint32_t qa[4], qb[4];
+                    decode8(pa[m], qa);
+                    decode8(pb[m], qb);
+                    const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
+                    const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
+#pragma unroll
+                    for (int nb = 0; nb < NNB; ++nb) {
+                        float p[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma16816(p, a0, hb[nb].x, hb[nb].y);
+                        mma16816(p, a1, hb[nb].z, hb[nb].w);
+                        acc[m][nb][0] = fmaf(p[0], fa, acc[m][nb][0]);
+                        acc[m][nb][1] = fmaf(p[1], fa, acc[m][nb][1]);
+                        acc[m][nb][2] = fmaf(p[2], fb, acc[m][nb][2]);
+                        acc[m][nb][3] = fmaf(p[3], fb, acc[m][nb][3]);
+                    }
+                }
+            }
+        }
+    }
+    return true;
+}
 
 template <int NMAT, int NS, int MODE>
 __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_constant__ CUtensorMap bmap,
@@ -146,24 +209,17 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
         // ------------------------------------------------------------ consumers
         const int cw = warp - 1;                 // 0..7: rows 16 cw .. 16 cw + 15 of the 128-row block
         const int g8 = lane >> 2, c = lane & 3;
-        const int ra_l = 16 * cw + g8, rb_l = ra_l + 8;       // local rows (ra_l & 7 == g8)
+        const int ra_l = 16 * cw + g8;           // local rows ra_l and ra_l + 8 (both = g8 mod 8)
         uint32_t it = 0;
         for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
             const int4 tile = __ldg(a.tiles + t / m_tiles);
             const int grp = tile.x, b_first = tile.y, nt = tile.z;
             const int m0 = (t % m_tiles) * 128;
-            const int ra = m0 + ra_l, rb = m0 + rb_l;
-            const uint8_t *sa[NMAT], *sb[NMAT];
-            int ea[NMAT], eb[NMAT];
+            const int ra = m0 + ra_l, rb = ra + 8;
+            const uint2 *sa[NMAT];               // row ra's scale bytes; row rb's follow 8 rows later
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-                const uint8_t *S = a.scales[m][grp];
-                sa[m] = S + (size_t)ra * kb;
-                sb[m] = S + (size_t)rb * kb;
-                ea[m] = __ldg(a.rowmax[m] + (size_t)grp * a.rows + ra);
-                eb[m] = __ldg(a.rowmax[m] + (size_t)grp * a.rows + rb);
-            }
-            const int nnb = (nt + 7) >> 3;           // n-blocks of 8 tokens (<= 2)
+            for (int m = 0; m < NMAT; ++m)
+                sa[m] = reinterpret_cast<const uint2 *>(a.scales[m][grp] + (size_t)ra * kb);
             float acc[NMAT][2][4];
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
@@ -171,87 +227,10 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) acc[m][h][q] = 0.f;
-            // scale bytes: 8 per row and stage (blocks 8s .. 8s+7), read one stage ahead
-            uint2 sca[NMAT], scb[NMAT], nsa[NMAT], nsb[NMAT];
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-                nsa[m] = __ldg(reinterpret_cast<const uint2 *>(sa[m]));
-                nsb[m] = __ldg(reinterpret_cast<const uint2 *>(sb[m]));
-            }
-            bool ok = true;
-            for (int s = 0; s < nkp; ++s, ++it) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    sca[m] = nsa[m];
-                    scb[m] = nsb[m];
-                    if (s + 1 < nkp) {
-                        nsa[m] = __ldg(reinterpret_cast<const uint2 *>(sa[m]) + s + 1);
-                        nsb[m] = __ldg(reinterpret_cast<const uint2 *>(sb[m]) + s + 1);
-                    }
-                }
-                const int slot = it % NS;
-                if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, 0xFFFFFFFFu, a.status, 12)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *sbase = smem + slot * SM::STAGE;
-                const uint8_t *bbase = sbase + NMAT * GV_STAGE_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    // this thread's bytes: rows ra/rb, bytes [32 ks + 8 c, +8) of the 128-byte row
-                    uint2 pa[NMAT], pb[NMAT];
-                    const int chunk = 2 * ks + (c >> 1);
-#pragma unroll
-                    for (int m = 0; m < NMAT; ++m) {
-                        const uint8_t *base = sbase + m * GV_STAGE_BYTES;
-                        pa[m] = *reinterpret_cast<const uint2 *>(base + ra_l * 128 + 16 * (chunk ^ (ra_l & 7)) + 8 * (c & 1));
-                        pb[m] = *reinterpret_cast<const uint2 *>(base + rb_l * 128 + 16 * (chunk ^ (rb_l & 7)) + 8 * (c & 1));
-                    }
-                    // activation fragments of tokens 8 nb + g8: K = 64 ks + 16 c .. + 15 of this
-                    // stage = 16-byte chunks 2c, 2c+1 of row (8 nb + g8) in box ks (128-byte swizzle)
-                    uint4 hb[2][2];
-#pragma unroll
-                    for (int nb = 0; nb < 2; ++nb) {
-                        if (nb < nnb) {                  // tokens 8..15 only when the tile has them
-                            const int br = 8 * nb + g8;
-                            const uint8_t *bx = bbase + ks * 16 * 128 + br * 128;
-                            hb[nb][0] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c) ^ (br & 7)));
-                            hb[nb][1] = *reinterpret_cast<const uint4 *>(bx + 16 * ((2 * c + 1) ^ (br & 7)));
-                        }
-                    }
-                    if (ks == 3) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(empty + slot));
-                    }
-                    // block of this thread's codes in this stage: 2 ks + c / 2 (byte of the 8)
-                    const int bsh = 8 * (2 * (ks & 1) + (c >> 1));
-#pragma unroll
-                    for (int m = 0; m < NMAT; ++m) {
-                        const uint32_t wsa = (ks >> 1) ? sca[m].y : sca[m].x;
-                        const uint32_t wsb = (ks >> 1) ? scb[m].y : scb[m].x;
-                        const __half2 fa = pow2_h2((int)((wsa >> bsh) & 0xFF) - ea[m]);
-                        const __half2 fb = pow2_h2((int)((wsb >> bsh) & 0xFF) - eb[m]);
-                        uint32_t qa[8], qb[8];
-                        decode8(pa[m].x, fa, *reinterpret_cast<uint32_t(*)[4]>(&qa[0]));
-                        decode8(pa[m].y, fa, *reinterpret_cast<uint32_t(*)[4]>(&qa[4]));
-                        decode8(pb[m].x, fb, *reinterpret_cast<uint32_t(*)[4]>(&qb[0]));
-                        decode8(pb[m].y, fb, *reinterpret_cast<uint32_t(*)[4]>(&qb[4]));
-#pragma unroll
-                        for (int st = 0; st < 4; ++st) {
-                            const uint32_t af[4] = {qa[2 * st], qb[2 * st], qa[2 * st + 1], qb[2 * st + 1]};
-#pragma unroll
-                            for (int nb = 0; nb < 2; ++nb) {
-                                if (nb < nnb) {
-                                    const uint4 &h0 = hb[nb][st >> 1];
-                                    const uint32_t b0 = (st & 1) ? h0.z : h0.x, b1 = (st & 1) ? h0.w : h0.y;
-                                    mma16816(acc[m][nb], af, b0, b1);
-                                }
-                            }
-                        }
-                    }
-                }
-            }
+            const bool ok = nt > 8 ? gemv_k_loop<NMAT, NS, 2>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
+                                                              sa, kb, it, acc)
+                                   : gemv_k_loop<NMAT, NS, 1>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
+                                                              sa, kb, it, acc);
             if (!ok) break;
             // epilogue: acc[m][nb][0..1] = (row ra, tokens 8 nb + 2c, +1); [2..3] = (row rb, same tokens)
 #pragma unroll
@@ -262,18 +241,16 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                     const int row = (q < 2) ? ra : rb;
                     if (tok < nt) {
                         const size_t orow = (size_t)(b_first + tok);
-                        const float f0 = e8m0_to_f32((uint32_t)((q < 2) ? ea[0] : eb[0]));
                         if (MODE == GV_GLU_F16) {
-                            const float f1 = e8m0_to_f32((uint32_t)((q < 2) ? ea[NMAT - 1] : eb[NMAT - 1]));
                             const float rs = a.rscale ? __ldg(a.rscale + orow) : 1.f;
-                            const float gv = acc[0][nb][q] * f0 * rs;
-                            const float uv = acc[NMAT - 1][nb][q] * f1 * rs;
+                            const float gv = acc[0][nb][q] * rs;
+                            const float uv = acc[NMAT - 1][nb][q] * rs;
                             const float av = gv / (1.0f + expf(-gv)) * uv;
                             if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
                             reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
                         } else {
                             reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] =
-                                f32_to_bf16(acc[0][nb][q] * f0);
+                                f32_to_bf16(acc[0][nb][q]);
                         }
                     }
                 }

@@ -13,7 +13,6 @@ struct GemvArgs {
     int amap_stride;
     int amap_off[2];
     const uint8_t *const *scales[2];   // [groups] of scale matrices [rows, K/32]
-    const uint8_t *rowmax[2];          // [groups * rows] per-row max exponent byte
     int rows, K;                       // rows: multiple of 128; K: multiple of 512
     const int4 *tiles;                 // (group, first B row, B rows <= 16) per token tile
     const int *n_tiles;                // device count of tiles

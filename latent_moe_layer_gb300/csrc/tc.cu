@@ -443,8 +443,6 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g1.amap_off[1] = 1;
         g1.scales[0] = h->d_eptr[1];
         g1.scales[1] = h->d_eptr[3];
-        g1.rowmax[0] = rm;
-        g1.rowmax[1] = rm + (size_t)E * I;
         g1.rows = I;
         g1.K = L;
         g1.tiles = (const int4 *)ws.tiles;
@@ -455,7 +453,6 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         GemvArgs g2 = g1;
         g2.amap_off[0] = g2.amap_off[1] = 2;
         g2.scales[0] = g2.scales[1] = h->d_eptr[5];
-        g2.rowmax[0] = g2.rowmax[1] = rm + (size_t)2 * E * I;
         g2.rows = L;
         g2.K = I;
         g2.rscale = nullptr;
