@@ -8,7 +8,7 @@ write) between steps outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
-Default workload: the K3 decode batch of 16 tokens (configs[1]).  Under
+Default workload: the K3 decode batch of 16 tokens (--config 1).  Under
 torchrun every rank runs an independent replica on its own GPU (the layer is
 token-parallel; no collective on the data path); the time is the max over
 ranks and the value counts the tokens of all ranks.

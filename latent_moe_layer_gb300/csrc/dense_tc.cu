@@ -68,8 +68,10 @@ __device__ __forceinline__ DnTile dn_tile(const DenseArgs &args, int t, int mt_n
     t /= S.splits;
     r.m0 = (t % mt_n) * DN_BM;
     r.n0 = (t / mt_n) * BN;
-    r.ks = S.K / DN_BK / S.splits;
-    r.k0 = r.split * r.ks;
+    // split s of KS K steps covers [s KS / splits, (s + 1) KS / splits): sizes differ by at most one
+    const int KS = S.K / DN_BK;
+    r.k0 = r.split * KS / S.splits;
+    r.ks = (r.split + 1) * KS / S.splits - r.k0;
     return r;
 }
 

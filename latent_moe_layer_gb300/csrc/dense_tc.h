@@ -12,7 +12,7 @@ enum DenseOut { DN_OUT_F32 = 0, DN_OUT_BF16 = 1 };
 struct DenseSeg {
     int n_tiles;     // ceil(n_out / BN)
     int n_out;       // valid weight rows
-    int splits;      // split-K factor ((K / 64) % splits == 0)
+    int splits;      // split-K factor, 1 .. K / 64 (split s takes K steps [s KS / splits, (s + 1) KS / splits))
     int K;           // reduction length (multiple of 64)
     int a_kmod;      // X column = k % a_kmod (router hi/lo: H; otherwise K)
     int mode;        // DN_OUT_F32: out[(split * M + m) * ldo + col0 + n]; DN_OUT_BF16: out[m * ldo + col0 + n]

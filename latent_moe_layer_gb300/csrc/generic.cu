@@ -304,14 +304,22 @@ __global__ void __launch_bounds__(1024) combine_norm_v8_kernel(
 #pragma unroll
     for (int q = 0; q < 8; ++q) z[q] = 0.f;
     if (i < L) {
-        for (int k = 0; k < K; ++k) {      // fixed k order
-            const uint4 v = *reinterpret_cast<const uint4 *>(y + (size_t)rows[k] * L + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            const float wk = ws_[k];
+        // fixed k order; the rows of a group of 8 are loaded before they are summed
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            uint4 v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                z[2 * q] = fmaf(wk, __uint_as_float(w[q] << 16), z[2 * q]);
-                z[2 * q + 1] = fmaf(wk, __uint_as_float(w[q] & 0xffff0000u), z[2 * q + 1]);
+            for (int k = 0; k < 8; ++k)
+                if (k0 + k < K) v[k] = *reinterpret_cast<const uint4 *>(y + (size_t)rows[k0 + k] * L + i);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k0 + k >= K) break;
+                const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                const float wk = ws_[k0 + k];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    z[2 * q] = fmaf(wk, __uint_as_float(w[q] << 16), z[2 * q]);
+                    z[2 * q + 1] = fmaf(wk, __uint_as_float(w[q] & 0xffff0000u), z[2 * q + 1]);
+                }
             }
         }
     }

@@ -146,6 +146,9 @@ struct k3moe_handle {
     uint16_t *d_router_hilo = nullptr;         // tensor-path router weights as BF16 [E, 2H] (hi | lo)
     size_t tmap_count = 0;
     k3_prof *prof = nullptr;                   // stage timing, when enabled
+    // split-K plans of the decode-size dense GEMMs per token count (0 = not planned yet):
+    // [T][0] router, [T][1] down-projection, [T][2] up-projection
+    unsigned char dense_splits[257][3] = {};
 };
 
 // Stage bracket used by the forward orchestration.

@@ -43,7 +43,6 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ lrow, const 
     __syncwarp();
     uint32_t taken = 0;          // bit i: key lane + 32 i taken (owner lane's view)
     int sel_j = 0;
-    float ssum = 0.f;
     for (int s = 0; s < K; ++s) {
         float wk = bk;
         int wj = bj;
@@ -82,13 +81,15 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ lrow, const 
             bk = ck;
             bj = cj;
         }
-        const float l = lrow[wj];
-        ssum += 1.0f / (1.0f + expf(-l));
         if (lane == s) sel_j = wj;
     }
+    // weights: sigma(l) of the selected experts over their sum (a butterfly sum: every
+    // lane adds the same operand pairs, so all lanes hold the same total)
+    const float sg = lane < K ? 1.0f / (1.0f + expf(-lrow[sel_j])) : 0.f;
+    float ssum = sg;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
     if (lane < K) {
-        const float l = lrow[sel_j];
-        const float sg = 1.0f / (1.0f + expf(-l));
         idx_row[lane] = sel_j;
         w_row[lane] = sg / ssum * scaling;
         if (sidx) sidx[lane] = sel_j;
@@ -199,7 +200,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *__restri
 // Decode-size routing in one CTA (T <= 32 tokens, T K <= 1024 pairs, E <= 1024):
 // top-K per token (warp t), the expert histogram in shared memory, the scan and
 // tile list, and the stable scatter (a pair's row within its expert is the
-// number of earlier pairs, in (t, k) order, that chose the same expert).
+// number of earlier pairs, in (t, k) order, that chose the same expert: the
+// number of earlier tokens in the expert's token bit mask).
 template <int MAXP>
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const float *__restrict__ logits, const float *__restrict__ bias, int T, int E, int K, float scaling,
@@ -210,8 +212,10 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     griddep_enter();
     extern __shared__ float rs_keys[];                // [32][MAXP][32]
     __shared__ int s_idx[1024], s_hist[1024];
+    __shared__ uint32_t s_tok[1024];                 // bit t: token t selected expert e (T <= 32)
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, n = T * K;
     s_hist[tid] = 0;
+    s_tok[tid] = 0;
     __syncthreads();
     if (w < T)
         topk_warp<MAXP>(logits + (size_t)w * E, bias, E, K, scaling,
@@ -221,16 +225,18 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     if (tid < n) {
         const int e = s_idx[tid];
         if (e < 0 || e >= E) set_status(status, K3MOE_ERR_RANGE, e);
-        else atomicAdd(&s_hist[e], 1);
+        else {
+            atomicAdd(&s_hist[e], 1);
+            atomicOr(&s_tok[e], 1u << (tid / K));
+        }
     }
     __syncthreads();
     perm_scan_block(s_hist, E, tile_n, offsets, active, tiles, meta);
     if (tid < n) {
         const int e = s_idx[tid];
         if (e >= 0 && e < E) {
-            int rank = 0;
-            for (int q = 0; q < tid; ++q) rank += s_idx[q] == e;
-            const int row = offsets[e] + rank;
+            // a token selects an expert at most once: the earlier pairs on e are its earlier tokens
+            const int row = offsets[e] + __popc(s_tok[e] & ((1u << (tid / K)) - 1u));
             tok_of[row] = tid / K;
             row_of[tid] = row;
         }

@@ -1,6 +1,7 @@
 // Tensor-core path: TMA descriptors, load-time row maxima, activation prep and
 // the forward orchestration around the tcgen05 grouped expert GEMMs.
 #include <string.h>
+#include <algorithm>
 #include <vector>
 
 #include "tc.h"
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
     }
     const float up = __uint_as_float((uint32_t)(k + 127) << 23);
     const float down = __uint_as_float((uint32_t)(127 - k) << 23);
-    for (int kk = 0; kk < K; ++kk) {
+    for (int kk = blockIdx.y; kk < K; kk += gridDim.y) {     // this CTA's copies of the row
         const int row = row_of ? row_of[(size_t)t * K + kk] : t;
         __half *d = dst + (size_t)row * cols;
         for (int i = tid * 8; i < cols; i += 256 * 8) {
@@ -133,6 +134,15 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
         }
         if (tid == 0) rscale[row] = down;
     }
+}
+
+// CTAs per token for prep_f16_rows_kernel: the K copies of a row are spread
+// over up to K CTAs while the grid is below two CTAs per SM.
+static unsigned prep_split(int T, int K, int num_sms)
+{
+    int p = 1;
+    while (p < K && (long)T * p * 2 <= 2L * num_sms) p *= 2;
+    return (unsigned)std::min(p, K);
 }
 
 // Token tiles of a dense (all-token) GEMM: (0, row0, rows) with at most bn rows.
@@ -226,27 +236,64 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
     return K3MOE_OK;
 }
 
-// Split-K factor (dividing the K steps, <= K3_DENSE_MAX_SPLITS) whose CTAs each
-// stream close to `per_cta` K steps: every CTA of a launch then moves about the
-// same weight bytes, whichever segment it belongs to.
-static int choose_splits(int ksteps, double per_cta)
+// Split-K factors for one launch of the persistent dense GEMM (BN = 128 weight
+// rows per tile).  The kernel takes its units (segment 0's tiles first; per
+// tile its splits in order, the split sizes differing by at most one K step)
+// round-robin over `grid_max` CTAs.  Costs are in K steps (16 KB of weights):
+// a unit costs its K steps plus its fp32 partial tile (rows x 128 x 4 bytes =
+// rows / 32 K steps), and the reduction reads every partial once, spread over
+// the whole GPU.  The plan minimises the busiest CTA's load plus the
+// reduction; ties go to fewer units.
+static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max)
 {
-    int best = 1;
-    double err = 1e30;
-    for (int sp = 1; sp <= K3_DENSE_MAX_SPLITS; ++sp) {
-        if (ksteps % sp) continue;
-        const double e = fabs((double)ksteps / sp - per_cta);
-        if (e < err) {
-            err = e;
-            best = sp;
-        }
+    const int mt = (T + 127) / 128;
+    int ks_total[2], maxsp[2];
+    for (int s = 0; s < nseg; ++s) {
+        ks_total[s] = seg[s].K / 64;
+        maxsp[s] = std::min(K3_DENSE_MAX_SPLITS, ks_total[s]);
     }
-    return best;
+    std::vector<double> load;
+    double best = 1e30;
+    int best_units = 0, best_sp[2] = {1, 1};
+    for (int s0 = 1; s0 <= maxsp[0]; ++s0)
+        for (int s1 = 1; s1 <= (nseg > 1 ? maxsp[1] : 1); ++s1) {
+            const int sp[2] = {s0, s1};
+            int units = 0;
+            double reduce = 0;
+            for (int s = 0; s < nseg; ++s) {
+                units += seg[s].n_tiles * mt * sp[s];
+                reduce += (double)sp[s] * T * seg[s].n_out * 4.0;
+            }
+            const int grid = std::min(units, grid_max);
+            load.assign(grid, 0.0);
+            int u = 0;
+            for (int s = 0; s < nseg; ++s)
+                for (int t = 0; t < seg[s].n_tiles * mt * sp[s]; ++t, ++u) {
+                    const int k = t % sp[s], m = (t / sp[s]) % mt;
+                    const int rows = std::min(128, T - 128 * m);
+                    load[u % grid] += (k + 1) * ks_total[s] / sp[s] - k * ks_total[s] / sp[s] + rows / 32.0;
+                }
+            const double cost = *std::max_element(load.begin(), load.end()) + reduce / (16384.0 * grid_max);
+            if (cost < best - 1e-9 || (cost < best + 1e-9 && units < best_units)) {
+                best = cost;
+                best_units = units;
+                best_sp[0] = s0;
+                best_sp[1] = s1;
+            }
+        }
+    for (int s = 0; s < nseg; ++s) seg[s].splits = best_sp[s];
 }
 
-// K steps per CTA that spreads `tile_ksteps` (tiles x K steps, summed over the
-// launch's segments) over about two CTAs per SM.
-static double ksteps_per_cta(double tile_ksteps, int num_sms) { return tile_ksteps / (2.0 * num_sms); }
+// Cached per token count in the handle (the plan depends only on T and the shapes).
+static void dense_splits(k3moe_handle *h, DenseSeg *seg, int nseg, int T, int slot)
+{
+    unsigned char *c = h->dense_splits[T] + slot;
+    if (!c[0]) {
+        plan_splits(seg, nseg, T, 2 * h->num_sms);
+        for (int s = 0; s < nseg; ++s) c[s] = (unsigned char)seg[s].splits;
+    }
+    for (int s = 0; s < nseg; ++s) seg[s].splits = c[s];
+}
 
 // Decode-size token counts use BN = 128 tiles and split-K into fp32 partials
 // (two CTAs per SM); larger counts use BN = 256 tiles writing outputs directly.
@@ -284,11 +331,8 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     d.K = H;
     d.a_kmod = H;
     if (small) {
-        // split both segments so every CTA streams about the same weight bytes
-        const double per = ksteps_per_cta((double)mt * (r.n_tiles * (r.K / 64) + d.n_tiles * (d.K / 64)),
-                                          h->num_sms);
-        r.splits = choose_splits(r.K / 64, per);
-        d.splits = choose_splits(d.K / 64, per);
+        // split both segments so that the busiest CTA streams as few weight bytes as possible
+        dense_splits(h, a.seg, 2, T, 0);
         // partial columns: router [0, Ep), down [Ep, Ep + L); Ep rounds E to 16 floats
         r.mode = d.mode = DN_OUT_F32;
         r.out = d.out = ws.part;
@@ -343,7 +387,8 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.mode = (!small && out16) ? DN_OUT_BF16 : DN_OUT_F32;
     u.col0 = 0;
     u.ldo = H;
-    u.splits = small ? choose_splits(L / 64, ksteps_per_cta((double)mt * u.n_tiles * (L / 64), h->num_sms)) : 1;
+    u.splits = 1;
+    if (small) dense_splits(h, a.seg, 1, T, 2);
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
     int rc = k3_launch_dense_tc(bn, an, bu, bu, a, h->num_sms, st);
     if (rc) return rc;
@@ -401,7 +446,8 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     if ((rc = k3_launch_route(h, ws, T, gemv ? 16 : bn, st))) return rc;
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
-        k3_launch(prep_f16_rows_kernel, T, 256, 0, st, ws.h, L, ws.row_of, K, (__half *)ws.hperm, ws.hscale);
+        k3_launch(prep_f16_rows_kernel, dim3(T, prep_split(T, K, h->num_sms)), 256, 0, st, ws.h, L, ws.row_of, K,
+                  (__half *)ws.hperm, ws.hscale);
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
