@@ -437,6 +437,51 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def library_peaks(steps=50):
+    """Context numbers for the roofline discussion (not used by the layer): dense
+    GEMM throughput of the vendor library on this GPU at 8192^3 -- BF16
+    (torch.matmul), FP8 E4M3 with per-tensor scales and, where this PyTorch build
+    exposes it, MXFP8 (E4M3 with E8M0 scales per 32 values) through
+    torch._scaled_mm.  Prints one JSON line."""
+    import torch
+    n = 8192
+    out = {"shape": [n, n, n]}
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return round(2.0 * n ** 3 / (e0.elapsed_time(e1) / steps * 1e-3) / 1e12, 1)
+
+    a = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    b = torch.randn(n, n, device="cuda", dtype=torch.bfloat16)
+    out["bf16_tflops"] = timed(lambda: a @ b)
+    a8 = a.to(torch.float8_e4m3fn)
+    b8 = b.to(torch.float8_e4m3fn).t().contiguous().t()      # column-major second operand
+    one = torch.ones((), device="cuda", dtype=torch.float32)
+    try:
+        out["fp8_tensorwise_tflops"] = timed(lambda: torch._scaled_mm(a8, b8, one, one, out_dtype=torch.bfloat16))
+    except Exception as ex:                                     # noqa: BLE001
+        out["fp8_tensorwise_tflops"] = None
+        out["fp8_tensorwise_error"] = str(ex).splitlines()[0][:200]
+    try:
+        e8 = getattr(torch, "float8_e8m0fnu")
+        sa = torch.full((n, n // 32), 127, device="cuda", dtype=torch.uint8).view(e8)
+        sb = torch.full((n, n // 32), 127, device="cuda", dtype=torch.uint8).view(e8)
+        out["mxfp8_tflops"] = timed(lambda: torch._scaled_mm(a8, b8, sa, sb, out_dtype=torch.bfloat16))
+    except Exception as ex:                                     # noqa: BLE001
+        out["mxfp8_tflops"] = None
+        out["mxfp8_error"] = str(ex).splitlines()[0][:200]
+    out["device"] = torch.cuda.get_device_name(0)
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,7 +494,12 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling aid)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--library-peaks", action="store_true",
+                    help="print the vendor library's dense BF16 / FP8 / MXFP8 GEMM rates and exit")
     args = ap.parse_args()
+    if args.library_peaks:
+        library_peaks()
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

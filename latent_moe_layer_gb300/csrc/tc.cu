@@ -168,7 +168,6 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
 
-// Tile shape by the token count per expert: small N for decode batches.
 // Tile shape by rows per expert: decode batches (<= 24 on average) take the
 // GEMV; up to 192 on average (partly filled tiles) take 192-token tiles with the
 // decoded weights in TMEM, which keeps shared memory below its bandwidth limit;
