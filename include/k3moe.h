@@ -141,7 +141,11 @@ size_t k3moe_workspace_bytes(const k3moe_handle *h, int T);
  * (optional, may be NULL) receive the selected experts in selection order and
  * their mixture weights.  T == 0 is a no-op.  Asynchronous on `stream`; the
  * workspace must not be used by anything else until the stream reaches this
- * point.
+ * point.  The call only enqueues kernels on `stream` (no host synchronisation,
+ * no allocation), so it may be recorded into a CUDA graph by stream capture
+ * and replayed while x, out, idx_out, w_out and the workspace stay where they
+ * were at capture (the first call per token count should run outside a
+ * capture: it sets kernel attributes).
  */
 int k3moe_forward(k3moe_handle *h, const void *x, int T, void *out, int32_t *idx_out,
                   float *w_out, void *workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -110,6 +110,34 @@ def test_tensor_and_generic_paths_agree():
     assert err < 2e-2
 
 
+@pytest.mark.parametrize("path,T", [(TEN, 16), (TEN, 300), (TEN, 2000), (GEN, 40)],
+                         ids=["tensor_gemv", "tensor_tmem_a", "tensor_256", "generic"])
+def test_forward_replays_from_a_cuda_graph(path, T):
+    # the forward enqueues only stream work (no host synchronisation, no allocation),
+    # so a captured graph replays it; outputs match the eager call bit for bit
+    cfg = synth.SMALL_ALIGNED.with_tokens(T)
+    dw = device_weights(cfg)
+    layer = k3moe.Layer(cfg, path=path)
+    layer.load(dw)
+    x = torch.from_numpy(synth.gen_x(cfg).view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    ws = layer.workspace(T)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward(x, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(x, out=out, workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert layer.status() == 0
+
+
 def test_batch_invariance():
     cfg = synth.SMALL_ALIGNED.with_tokens(37)
     full = run_gpu(cfg, AUTO)
