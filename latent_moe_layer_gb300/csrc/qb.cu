@@ -53,14 +53,51 @@ __device__ __forceinline__ float qb_warp_max(float v, int lane, int *who)
     return m;
 }
 
+// Bitonic sort of one value per lane, descending over the lanes (lane 0 the largest).
+__device__ __forceinline__ float qb_sort32_desc(float v, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool desc = (lane & k) == 0, low = (lane & j) == 0;
+            v = (low == desc) ? fmaxf(v, o) : fminf(v, o);
+        }
+    return v;
+}
+
+// Bitonic sort of 64 values (element i = lane + 32 h in c[h]), descending in i.
+__device__ __forceinline__ void qb_sort64_desc(float (&c)[2], int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j == 32) {                   // partners in the same lane (k = 64: descending)
+                const float hi = fmaxf(c[0], c[1]), lo = fminf(c[0], c[1]);
+                c[0] = hi;
+                c[1] = lo;
+                continue;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                const float o = __shfl_xor_sync(0xffffffffu, c[h], j);
+                const bool desc = (i & k) == 0, low = (i & j) == 0;
+                c[h] = (low == desc) ? fmaxf(c[h], o) : fminf(c[h], o);
+            }
+        }
+}
+
 // One warp per token (QB_TPW tokens per warp in turn).  The (K+1)-th largest
 // key is found among the keys not below L, the (K+1)-th largest of the 32
-// per-lane maxima (at least K+1 keys reach L, so alpha >= L): usually a few
-// dozen candidates, at most two per lane after compaction, from which K + 1
-// rounds remove the largest.  More than 64 candidates (heavy ties) or K + 1 >
+// per-lane maxima (at least K+1 keys reach L, so alpha >= L; a bitonic sort
+// of the lane maxima gives L): usually a few dozen candidates, at most two per
+// lane after compaction, sorted by a 64-element bitonic network.  More than 64 candidates (heavy ties) or K + 1 >
 // 32 fall back to rounds over every key.  The margin range is reduced over the
 // CTA and folded into the global range with one atomic pair per CTA.
-constexpr int QB_TPW = 4;
+constexpr int QB_TPW = 1;
 template <int MAXP>
 __global__ void __launch_bounds__(256) qb_alpha_kernel(const float *__restrict__ logits,
                                                        const float *__restrict__ bias, int T, int E, int K,
@@ -88,6 +125,7 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float *__restrict__
                 smax = fmaxf(smax, s);
                 smin = fminf(smin, s);
                 key = s + (bias ? bias[j] : 0.f);
+                if (key != key) key = -INFINITY;         // a NaN logit never selects
             }
             skey[wl][p][lane] = key;
             lmax = fmaxf(lmax, key);
@@ -98,11 +136,7 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float *__restrict__
         bool done = false;
         if (K + 1 <= 32) {
             // L: the (K+1)-th largest lane maximum
-            float v = lmax, L = -INFINITY;
-            for (int round = 0; round <= K; ++round) {
-                L = qb_warp_max(v, lane, &who);
-                if (lane == who) v = -INFINITY;
-            }
+            const float L = __shfl_sync(0xffffffffu, qb_sort32_desc(lmax, lane), K);
             // compact the keys >= L
             int c = 0;
             for (int p = 0; p < MAXP; ++p) c += skey[wl][p][lane] >= L;
@@ -119,15 +153,10 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float *__restrict__
                     if (k >= L) cand[wl][pos++] = k;
                 }
                 __syncwarp();
-                float c0 = lane < total ? cand[wl][lane] : -INFINITY;
-                float c1 = lane + 32 < total ? cand[wl][lane + 32] : -INFINITY;
-                for (int round = 0; round <= K; ++round) {
-                    a = qb_warp_max(fmaxf(c0, c1), lane, &who);
-                    if (lane == who) {
-                        if (c0 >= c1) c0 = -INFINITY;
-                        else c1 = -INFINITY;
-                    }
-                }
+                float cv[2] = {lane < total ? cand[wl][lane] : -INFINITY,
+                               lane + 32 < total ? cand[wl][lane + 32] : -INFINITY};
+                qb_sort64_desc(cv, lane);
+                a = __shfl_sync(0xffffffffu, cv[K >> 5], K & 31);   // K < 32 here
                 __syncwarp();
                 done = true;
             }
