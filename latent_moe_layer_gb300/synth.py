@@ -62,6 +62,9 @@ class LayerConfig:
     select_bias: bool = False
     rms_eps: float = 1e-6
     routed_scaling: float = 1.0
+    act: str = "silu"             # "silu" or "situ" (the GLU activation)
+    situ_beta: float = 4.0
+    situ_linear_beta: float = 25.0
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     def with_tokens(self, T: int) -> "LayerConfig":
@@ -72,6 +75,11 @@ class LayerConfig:
     def with_shared(self, S: int) -> "LayerConfig":
         d = dict(self.__dict__)
         d["S"] = S
+        return LayerConfig(**d)
+
+    def with_act(self, act: str) -> "LayerConfig":
+        d = dict(self.__dict__)
+        d["act"] = act
         return LayerConfig(**d)
 
 

@@ -26,12 +26,24 @@
  *      and the review's "Stable LatentMoE" section (routed path: down
  *      projection -> gated experts -> aggregation -> normalisation -> up
  *      projection): h = W_down x; per selected expert y_e = W2 (act(W1 h) * W3 h)
- *      with act = SiLU (w1 = gate, w3 = up); z = sum_k w_k y_k;
+ *      with act = SiLU (w1 = gate, w3 = up), or the SiTU reading below;
+ *      z = sum_k w_k y_k;
  *      n = z / sqrt(mean(z^2) + eps) * gamma (routed_expert_norm, RMSNorm before
  *      the up-projection); o = W_up n.
  *   4. Shared experts (optional).  The review's parameter section: two shared
  *      experts always on, on the full 7168 hidden, merged into one GLU of width
  *      2 x 3072 = 6144; o += W2s (act(W1s x) * W3s x).
+ *
+ *   5. SiTU-GLU (optional activation).  "Kimi K3, as released", section "What
+ *      is new since Kimi-Linear", item 3 (hidden_act "situ", Sigmoid Tanh Unit,
+ *      activation_situ_beta 4, activation_situ_linear_beta 25) and the review's
+ *      "SiTU-GLU is a soft fuse" section (sigmoid and tanh soft limits on the
+ *      two GLU branches; each output coordinate bounded by 100; near the origin
+ *      beta tanh(z/beta) = z + O(z^3/beta^2), so the unit is locally SwiGLU).
+ *      The pages print no formula.  Reading: SiLU's linear factor g is
+ *      soft-limited, and so is the linear (up) branch:
+ *        act(g, u) = sigmoid(g) * beta tanh(g/beta) * linear_beta tanh(u/linear_beta).
+ *      Parity unpinned beyond the bound and the two limits the pages state.
  *
  * Precision: inputs widen exactly (BF16/fp32 -> fp64); all arithmetic is fp64.
  */
@@ -98,6 +110,8 @@ typedef struct {
     double rms_eps, routed_scaling;
     int router_bf16;             /* 1: W_router holds BF16 bits; 0: fp32 */
     int has_bias;
+    int act;                     /* 0: SiLU; 1: SiTU */
+    double situ_beta, situ_linear_beta;
 } oracle_cfg;
 
 typedef struct {
@@ -122,6 +136,13 @@ static double router_weight(const oracle_cfg *c, const oracle_weights *w, int j,
 
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
 static double silu(double v) { return v * sigmoid(v); }
+
+/* The GLU activation of gate g and up u (step 3; step 5 for SiTU). */
+double oracle_act(int act, double beta, double linear_beta, double g, double u)
+{
+    if (act == 1) return sigmoid(g) * beta * tanh(g / beta) * linear_beta * tanh(u / linear_beta);
+    return silu(g) * u;
+}
 
 /* ------------------------------------------------------------ router */
 
@@ -195,8 +216,8 @@ void oracle_route(const oracle_cfg *c, const oracle_weights *w, const uint16_t *
  * out[t] += coef[t] * W2 (act(W1 in[t]) * W3 in[t]) for t < ntok, with the three
  * MXFP4 matrices dequantised row by row.  in: [ntok][din], out: [ntok][dout].
  */
-static void glu_apply(const uint8_t *w1p, const uint8_t *w1s, const uint8_t *w3p, const uint8_t *w3s,
-                      const uint8_t *w2p, const uint8_t *w2s, int din, int dint, int dout,
+static void glu_apply(const oracle_cfg *c, const uint8_t *w1p, const uint8_t *w1s, const uint8_t *w3p,
+                      const uint8_t *w3s, const uint8_t *w2p, const uint8_t *w2s, int din, int dint, int dout,
                       int ntok, const double *in, const double *coef, double *out)
 {
     double *a = (double *)malloc(sizeof(double) * (size_t)ntok * dint);
@@ -220,7 +241,7 @@ static void glu_apply(const uint8_t *w1p, const uint8_t *w1s, const uint8_t *w3p
                     g += r1[k] * v[k];
                     u += r3[k] * v[k];
                 }
-                a[(size_t)t * dint + r] = silu(g) * u;
+                a[(size_t)t * dint + r] = oracle_act(c->act, c->situ_beta, c->situ_linear_beta, g, u);
             }
         }
         free(r1);
@@ -319,7 +340,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
         if (rc)
             break;
         memset(y, 0, sizeof(double) * (size_t)m * L);
-        glu_apply(w->w1p[e], w->w1s[e], w->w3p[e], w->w3s[e], w->w2p[e], w->w2s[e],
+        glu_apply(c, w->w1p[e], w->w1s[e], w->w3p[e], w->w3s[e], w->w2p[e], w->w2s[e],
                   L, c->I, L, m, in, coef, y);
         for (int q = 0; q < m; q++)
             for (int r = 0; r < L; r++)
@@ -355,7 +376,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
         double *ones = (double *)malloc(sizeof(double) * n);
         for (int i = 0; i < n; i++)
             ones[i] = 1.0;
-        glu_apply(w->ws1p, w->ws1s, w->ws3p, w->ws3s, w->ws2p, w->ws2s, H, c->S, H, n, xin, ones, out);
+        glu_apply(c, w->ws1p, w->ws1s, w->ws3p, w->ws3s, w->ws2p, w->ws2s, H, c->S, H, n, xin, ones, out);
         free(ones);
     }
 

@@ -34,7 +34,8 @@ def build(force: bool = False) -> str:
 class _Cfg(C.Structure):
     _fields_ = [("H", C.c_int), ("L", C.c_int), ("E", C.c_int), ("K", C.c_int),
                 ("I", C.c_int), ("S", C.c_int), ("rms_eps", C.c_double),
-                ("routed_scaling", C.c_double), ("router_bf16", C.c_int), ("has_bias", C.c_int)]
+                ("routed_scaling", C.c_double), ("router_bf16", C.c_int), ("has_bias", C.c_int),
+                ("act", C.c_int), ("situ_beta", C.c_double), ("situ_linear_beta", C.c_double)]
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -71,6 +72,8 @@ def lib():
                                             C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_int]
             _lib.oracle_max_threads.restype = C.c_int
+            _lib.oracle_act.restype = d
+            _lib.oracle_act.argtypes = [C.c_int, d, d, d, d]
     return _lib
 
 
@@ -120,8 +123,10 @@ class _Keep:
 
 
 def _cfg(cfg) -> _Cfg:
+    act = {"silu": 0, "situ": 1}[getattr(cfg, "act", "silu")]
     return _Cfg(cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S, cfg.rms_eps, cfg.routed_scaling,
-                1 if cfg.router_dtype == "bf16" else 0, 1 if cfg.select_bias else 0)
+                1 if cfg.router_dtype == "bf16" else 0, 1 if cfg.select_bias else 0, act,
+                getattr(cfg, "situ_beta", 4.0), getattr(cfg, "situ_linear_beta", 25.0))
 
 
 def _weights(cfg, dense, experts, keep) -> _W:
@@ -142,6 +147,15 @@ def _weights(cfg, dense, experts, keep) -> _W:
     return _W(c(dense.w_router), c(dense.select_bias), c(dense.w_down), c(dense.w_up),
               c(dense.gamma), pp(tabs[0]), pp(tabs[1]), pp(tabs[2]), pp(tabs[3]), pp(tabs[4]),
               pp(tabs[5]), *sh)
+
+
+def act(kind: str, g, u, beta: float = 4.0, linear_beta: float = 25.0):
+    """The oracle's GLU activation a(g, u) ("silu" or the "situ" reading), elementwise."""
+    f = lib().oracle_act
+    k = {"silu": 0, "situ": 1}[kind]
+    g, u = np.broadcast_arrays(np.asarray(g, np.float64), np.asarray(u, np.float64))
+    return np.array([f(k, beta, linear_beta, float(a), float(b)) for a, b in zip(g.ravel(), u.ravel())]
+                    ).reshape(g.shape)
 
 
 def route(cfg, dense, x_rows: np.ndarray, nthreads: int = 0, want_logits: bool = False):
