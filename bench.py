@@ -51,6 +51,8 @@ def workload_name(cfg):
         s += f", shared GLU {cfg.H}->{cfg.S}->{cfg.H} MXFP4"
     if cfg.select_bias:
         s += ", Zipf(1.1) selection bias"
+    if getattr(cfg, "act", "silu") != "silu":
+        s += f", {cfg.act} GLU"
     return s
 
 
@@ -228,6 +230,8 @@ def run_ours(args):
         cfg = synth.LayerConfig(**{**cfg.__dict__, "E": args.experts, "name": cfg.name + f"_E{args.experts}"})
     if args.tokens:
         cfg = synth.LayerConfig(**{**cfg.__dict__, "T": args.tokens, "name": cfg.name + f"_T{args.tokens}"})
+    if args.act != "silu":
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "act": args.act, "name": cfg.name + f"_{args.act}"})
     pk, pk_src = peaks()
 
     dw = k3moe.DeviceWeights(cfg)
@@ -494,6 +498,8 @@ def main():
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling aid)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling aid)")
+    ap.add_argument("--act", default="silu", choices=["silu", "situ"],
+                    help="GLU activation (the workload's is SiLU; SiTU is the option the layer also supports)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--library-peaks", action="store_true",

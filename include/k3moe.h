@@ -57,7 +57,17 @@ extern "C" {
 #define K3MOE_ERR_STATE        -11   /* call out of order (e.g. forward before load_weights) */
 
 /* ------------------------------------------------------------ enums */
-#define K3MOE_ACT_SILU          0    /* act(g) = g * sigmoid(g) */
+#define K3MOE_ACT_SILU          0    /* a = g * sigmoid(g) * u */
+/* SiTU-GLU ("Kimi K3, as released", section "What is new since Kimi-Linear",
+ * item 3: hidden_act "situ", activation_situ_beta 4.0, activation_situ_linear_beta
+ * 25.0; the K3 report review, section "SiTU-GLU is a soft fuse": sigmoid and tanh
+ * soft limits on the two GLU branches, each output coordinate bounded by 100,
+ * beta tanh(z / beta) = z + O(z^3 / beta^2) near the origin).  The pages give no
+ * formula; this library reads it as
+ *   a = sigmoid(g) * beta tanh(g / beta) * linear_beta tanh(u / linear_beta),
+ * i.e. SiLU with its linear factor g soft-limited, times the soft-limited up
+ * branch (|a| < beta * linear_beta). */
+#define K3MOE_ACT_SITU          1
 
 #define K3MOE_ROUTER_F32        0    /* W_router stored fp32 (the K3 checkpoint's router) */
 #define K3MOE_ROUTER_BF16       1    /* W_router stored BF16 */
@@ -80,6 +90,8 @@ typedef struct k3moe_config {
     int router_dtype;    /* K3MOE_ROUTER_* */
     int has_select_bias; /* 1: key = sigmoid(l) + b, b given in k3moe_weights.select_bias */
     int path;            /* K3MOE_PATH_* */
+    float situ_beta;        /* K3MOE_ACT_SITU gate-branch beta (<= 0: 4.0) */
+    float situ_linear_beta; /* K3MOE_ACT_SITU up-branch beta (<= 0: 25.0) */
 } k3moe_config;
 
 /*

@@ -113,13 +113,16 @@ int k3moe_create(const k3moe_config *cfg, k3moe_handle **out)
     if (c.hidden % 32 || c.latent % 32 || c.inter % 32 || c.shared_inter % 32) return K3MOE_ERR_SHAPE;
     if (c.n_experts > 1024 || c.top_k > 32 || c.top_k > c.n_experts) return K3MOE_ERR_SHAPE;
     if (c.latent > 8192) return K3MOE_ERR_SHAPE;
-    if (c.act != K3MOE_ACT_SILU) return K3MOE_ERR_UNSUPPORTED;
+    if (c.act != K3MOE_ACT_SILU && c.act != K3MOE_ACT_SITU) return K3MOE_ERR_UNSUPPORTED;
+    if (!(c.situ_beta == c.situ_beta) || !(c.situ_linear_beta == c.situ_linear_beta)) return K3MOE_ERR_ARG;
     if (c.router_dtype != K3MOE_ROUTER_F32 && c.router_dtype != K3MOE_ROUTER_BF16) return K3MOE_ERR_ARG;
     if (c.path < K3MOE_PATH_AUTO || c.path > K3MOE_PATH_TENSOR) return K3MOE_ERR_ARG;
     if (!(c.rms_eps >= 0.f) || !(c.routed_scaling == c.routed_scaling)) return K3MOE_ERR_ARG;
     k3moe_handle *h = new (std::nothrow) k3moe_handle();
     if (!h) return K3MOE_ERR_ARG;
     h->cfg = c;
+    if (!(h->cfg.situ_beta > 0.f)) h->cfg.situ_beta = 4.0f;                 // the released config's values
+    if (!(h->cfg.situ_linear_beta > 0.f)) h->cfg.situ_linear_beta = 25.0f;
     *out = h;
     return K3MOE_OK;
 }
@@ -360,7 +363,7 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
     if ((rc = k3_launch_route(h, ws, T, 0, st))) return rc;   // top-K and the permutation
     {
         k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
-        if ((rc = k3_launch_glu_generic(ws.h, L, ws.tok_of, R, h->d_eptr[0], h->d_eptr[1], h->d_eptr[2],
+        if ((rc = k3_launch_glu_generic(k3_act_of(h->cfg), ws.h, L, ws.tok_of, R, h->d_eptr[0], h->d_eptr[1], h->d_eptr[2],
                                         h->d_eptr[3], ws.offsets, E, I, (float *)ws.act, h->d_status,
                                         st)))
             return rc;
@@ -385,7 +388,7 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
     if (c.shared_inter > 0) {
         k3_stage sg(h, K3MOE_STAGE_SHARED, st);
         const int S = c.shared_inter;
-        if ((rc = k3_launch_glu_generic((const uint16_t *)x, H, nullptr, T, k3_shared_tab(h, 0),
+        if ((rc = k3_launch_glu_generic(k3_act_of(h->cfg), (const uint16_t *)x, H, nullptr, T, k3_shared_tab(h, 0),
                                         k3_shared_tab(h, 1), k3_shared_tab(h, 2), k3_shared_tab(h, 3),
                                         nullptr, 1, S, (float *)ws.sact, h->d_status, st)))
             return rc;

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                             const float rs = a.rscale ? __ldg(a.rscale + orow) : 1.f;
                             const float gv = acc[0][nb][q] * rs;
                             const float uv = acc[NMAT - 1][nb][q] * rs;
-                            const float av = gv / (1.0f + expf(-gv)) * uv;
+                            const float av = k3_glu(gv, uv, a.act);
                             if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
                             reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
                         } else {

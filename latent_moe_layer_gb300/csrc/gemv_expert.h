@@ -17,6 +17,7 @@ struct GemvArgs {
     const int4 *tiles;                 // (group, first B row, B rows <= 16) per token tile
     const int *n_tiles;                // device count of tiles
     const float *rscale;               // [R] per-row factor applied to the GLU inputs, or nullptr
+    K3Act act;                         // GLU activation
     void *out;                         // GLU: f16 [R, rows]; BF16: BF16 [R, rows]
     int *status;
 };

@@ -1,7 +1,7 @@
 // Generic CUDA-core kernels: any shape whose widths are multiples of 32.
 //
 //   rows_gemm     out[m, n] (+)= sum_k A[m, k] W[n, k]        (router, down/up projections)
-//   glu_generic   act[r, i] = silu(W1_e[i] . in[tok(r)]) * (W3_e[i] . in[tok(r)])
+//   glu_generic   act[r, i] = a(W1_e[i] . in[tok(r)], W3_e[i] . in[tok(r)])  (SiLU or SiTU GLU)
 //   down_generic  y[r, o] (+)= W2_e[o] . act[r]
 //   combine_norm  n[t] = rmsnorm(sum_k w[t, k] y[row(t, k)]) * gamma
 //
@@ -125,7 +125,7 @@ __device__ __forceinline__ void decode_block(const uint8_t *p, uint32_t e, float
 // Grid (dint / 8, n_groups); warp w computes output row i = 8 * blockIdx.x + w for
 // every row r of the group, GX_TOK rows at a time; lanes split the K blocks.
 __global__ void __launch_bounds__(256) glu_generic_kernel(
-    const uint16_t *__restrict__ in, int din, const int32_t *__restrict__ row_token, int rows,
+    const K3Act act_fn, const uint16_t *__restrict__ in, int din, const int32_t *__restrict__ row_token, int rows,
     const uint8_t *const *__restrict__ w1p, const uint8_t *const *__restrict__ w1s,
     const uint8_t *const *__restrict__ w3p, const uint8_t *const *__restrict__ w3s,
     const int32_t *__restrict__ offsets, int dint, float *__restrict__ act)
@@ -179,8 +179,7 @@ __global__ void __launch_bounds__(256) glu_generic_kernel(
 #pragma unroll
             for (int t = 0; t < GX_TOK; ++t)
                 if (t == lane) { gv = gacc[t]; uv = uacc[t]; }
-            float sg = gv / (1.0f + expf(-gv));
-            act[(size_t)(rb + lane) * dint + i] = sg * uv;
+            act[(size_t)(rb + lane) * dint + i] = k3_glu(gv, uv, act_fn);
         }
     }
 }
@@ -402,7 +401,7 @@ int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, 
     return K3_LAUNCH_OK();
 }
 
-int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token, int rows,
+int k3_launch_glu_generic(const K3Act &act_fn, const uint16_t *in, int din, const int32_t *row_token, int rows,
                           const uint8_t *const *w1p, const uint8_t *const *w1s,
                           const uint8_t *const *w3p, const uint8_t *const *w3s,
                           const int32_t *offsets, int n_groups, int dint, float *act, int *status,
@@ -411,7 +410,8 @@ int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token,
     (void)status;
     if (n_groups > 65535) return K3MOE_ERR_UNSUPPORTED;
     dim3 grid((dint + 7) / 8, n_groups);
-    k3_launch(glu_generic_kernel, grid, 256, 0, st, in, din, row_token, rows, w1p, w1s, w3p, w3s, offsets, dint, act);
+    k3_launch(glu_generic_kernel, grid, 256, 0, st, act_fn, in, din, row_token, rows, w1p, w1s, w3p, w3s, offsets,
+              dint, act);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }

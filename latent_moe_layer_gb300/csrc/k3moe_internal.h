@@ -43,6 +43,23 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f)
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// GLU activation a(g, u) of one gate/up pair (K3MOE_ACT_*): SiLU g sigmoid(g) u,
+// or the SiTU reading sigmoid(g) beta tanh(g / beta) linear_beta tanh(u / linear_beta)
+// (the K3 report review, "SiTU-GLU is a soft fuse" section; constants from the
+// released config).  inv_* are the reciprocals of the betas.
+struct K3Act {
+    int kind;
+    float beta, linear_beta, inv_beta, inv_linear_beta;
+};
+
+__device__ __forceinline__ float k3_glu(float g, float u, const K3Act &a)
+{
+    const float sg = 1.0f / (1.0f + expf(-g));
+    if (a.kind == K3MOE_ACT_SITU)
+        return sg * a.beta * tanhf(g * a.inv_beta) * (a.linear_beta * tanhf(u * a.inv_linear_beta));
+    return g * sg * u;
+}
+
 // 2^(e-127) for an E8M0 byte e in [0, 254] (e = 0 gives the fp32 subnormal 2^-127).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e)
 {
@@ -124,6 +141,17 @@ struct k3_prof {
 };
 
 // --------------------------------------------------------------- host handle
+inline k3::K3Act k3_act_of(const k3moe_config &c)
+{
+    k3::K3Act a;
+    a.kind = c.act;
+    a.beta = c.situ_beta;
+    a.linear_beta = c.situ_linear_beta;
+    a.inv_beta = 1.0f / c.situ_beta;
+    a.inv_linear_beta = 1.0f / c.situ_linear_beta;
+    return a;
+}
+
 struct k3moe_handle {
     k3moe_config cfg;
     bool loaded = false;
@@ -228,7 +256,7 @@ int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStr
 // generic CUDA-core kernels (generic.cu)
 int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,
                         float *out_f32, uint16_t *out_bf16, int accumulate, cudaStream_t st);
-int k3_launch_glu_generic(const uint16_t *in, int din, const int32_t *row_token, int rows,
+int k3_launch_glu_generic(const k3::K3Act &act_fn, const uint16_t *in, int din, const int32_t *row_token, int rows,
                           const uint8_t *const *w1p, const uint8_t *const *w1s,
                           const uint8_t *const *w3p, const uint8_t *const *w3s,
                           const int32_t *offsets, int n_groups, int dint, float *act,

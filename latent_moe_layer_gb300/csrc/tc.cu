@@ -468,6 +468,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a1.tiles = (const int4 *)ws.tiles;
     a1.n_tiles = ws.meta + 1;
     a1.rscale = ws.hscale;
+    a1.act = k3_act_of(c);
     a1.out = ws.act;
     a1.status = h->d_status;
     a1.spin_limit = 0xFFFFFFFFu;
@@ -493,6 +494,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g1.tiles = (const int4 *)ws.tiles;
         g1.n_tiles = ws.meta + 1;
         g1.rscale = ws.hscale;
+        g1.act = k3_act_of(c);
         g1.out = ws.act;
         g1.status = h->d_status;
         GemvArgs g2 = g1;
@@ -557,6 +559,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         s1.tiles = stiles;
         s1.n_tiles = ws.meta + 2;
         s1.rscale = ws.xscale;
+        s1.act = k3_act_of(c);
         s1.out = ws.sact;
         ExpertGemmArgs s2 = s1;
         s2.amap_off[0] = s2.amap_off[1] = 2;

@@ -49,6 +49,7 @@ struct ExpertGemmArgs {
     const float *addend;             // BF16_ADD: fp32 [R, rows] added before the rounding to BF16
     int *status;
     uint32_t spin_limit;
+    K3Act act;                       // GLU activation
 };
 
 constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
@@ -452,6 +453,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             if (!role_wait(smem_u32(tfull + acc), (tc / NACC) & 1, abort_flag, lim, args.status, 7)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
+            const bool situ = MODE == OUT_GLU_F16 && args.act.kind == K3MOE_ACT_SITU;
             const int nchunks = (nrows + 15) >> 4;
             for (int c = half; c < nchunks; c += NEPI / 4) {
                 // BF16_ADD: the chunk's addends are read before the TMEM loads, so
@@ -476,11 +478,19 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                     if (n < nrows) {
                         const size_t orow = (size_t)(row0 + n);
                         if (MODE == OUT_GLU_F16) {
-                            // SiLU(gv) = gv * sigmoid(gv) = hv + hv * tanh(hv) with hv = gv / 2
+                            // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
+                            // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
+                            // beta tanh(gv / beta) and soft-limits the up branch the same way
                             const float rs = srs[n];
                             const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
-                            const float a = fmaf(hv, tanh_approx(hv), hv) * uv;
+                            float a;
+                            if (situ)
+                                a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
+                                    tanh_approx(hv * (2.0f * args.act.inv_beta)) *
+                                    (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
+                            else
+                                a = fmaf(hv, tanh_approx(hv), hv) * uv;
                             bad |= !(fabsf(a) <= 65504.f);
                             reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                         } else if (MODE == OUT_BF16) {

@@ -20,6 +20,7 @@ ERR = {0: "OK", -1: "ARG", -2: "SHAPE", -3: "ALIGN", -4: "BAD_SCALE", -5: "ALIAS
 ERR_CODE = {v: k for k, v in ERR.items()}
 PATH_AUTO, PATH_GENERIC, PATH_TENSOR = 0, 1, 2
 ROUTER_F32, ROUTER_BF16 = 0, 1
+ACT_SILU, ACT_SITU = 0, 1
 
 EXPORTS = ["k3moe_create", "k3moe_persistent_bytes", "k3moe_load_weights", "k3moe_workspace_bytes",
            "k3moe_forward", "k3moe_forward_host", "k3moe_status", "k3moe_destroy", "k3moe_strerror",
@@ -40,7 +41,8 @@ class Config(C.Structure):
     _fields_ = [("hidden", C.c_int), ("latent", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
                 ("inter", C.c_int), ("shared_inter", C.c_int), ("rms_eps", C.c_float),
                 ("routed_scaling", C.c_float), ("act", C.c_int), ("router_dtype", C.c_int),
-                ("has_select_bias", C.c_int), ("path", C.c_int)]
+                ("has_select_bias", C.c_int), ("path", C.c_int), ("situ_beta", C.c_float),
+                ("situ_linear_beta", C.c_float)]
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -113,9 +115,11 @@ def _ptr(t):
 
 def make_config(cfg, path=PATH_AUTO) -> Config:
     """k3moe_config from a synth.LayerConfig (or anything with the same fields)."""
-    return Config(cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S, cfg.rms_eps, cfg.routed_scaling, 0,
+    act = {"silu": ACT_SILU, "situ": ACT_SITU}[getattr(cfg, "act", "silu")]
+    return Config(cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S, cfg.rms_eps, cfg.routed_scaling, act,
                   ROUTER_BF16 if cfg.router_dtype == "bf16" else ROUTER_F32,
-                  1 if cfg.select_bias else 0, path)
+                  1 if cfg.select_bias else 0, path, getattr(cfg, "situ_beta", 4.0),
+                  getattr(cfg, "situ_linear_beta", 25.0))
 
 
 class Layer:

@@ -138,6 +138,24 @@ def test_forward_replays_from_a_cuda_graph(path, T):
     assert layer.status() == 0
 
 
+# The SiTU-GLU reading (sigmoid(g) 4 tanh(g / 4) * 25 tanh(u / 25)) on every GLU
+# kernel: generic, decode GEMV (T = 40), 192-token TMEM-A tiles (T = 300), 256-token
+# tiles (T = 1500), and the shared experts' tcgen05 GLU at N <= 32 and N = 256.
+@pytest.mark.parametrize("path,name,T", [(GEN, "SMALL_ALIGNED", 40), (TEN, "SMALL_ALIGNED", 40),
+                                         (TEN, "SMALL_ALIGNED", 300), (TEN, "SMALL_ALIGNED", 1500),
+                                         (GEN, "SMALL_SHARED", 40), (TEN, "SMALL_SHARED", 40),
+                                         (TEN, "SMALL_SHARED", 150)])
+def test_situ_parity(path, name, T):
+    cfg = getattr(synth, name).with_tokens(T).with_act("situ")
+    g = run_gpu(cfg, path)
+    assert g["status"] == 0 and g["path"] == path
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+    # and it is not the SiLU layer
+    silu = oracle_rows(cfg.with_act("silu"), device_weights(cfg).dense, g["x"])
+    assert np.abs(silu["out"] - ref["out"]).max() > 1e-3
+
+
 def test_batch_invariance():
     cfg = synth.SMALL_ALIGNED.with_tokens(37)
     full = run_gpu(cfg, AUTO)
@@ -252,8 +270,8 @@ def test_bounded_wait_times_out_and_context_survives():
 
 
 # ------------------------------------------------------------------ K3 sizes
-def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0):
-    cfg = synth.CONFIGS[cfg_id]
+def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0, act="silu"):
+    cfg = synth.CONFIGS[cfg_id].with_act(act)
     dw = device_weights(cfg)
     g = run_gpu(cfg, path, dw=dw)
     assert g["status"] == 0
@@ -277,6 +295,11 @@ def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0):
 def test_k3_decode_t16(path):
     g, _ = _k3_case(1, 16, 16, path=path)
     assert g["path"] == path
+
+
+def test_k3_decode_t16_situ():
+    # the SiTU reading on the decode GEMV at the K3 shapes (weights shared with the SiLU case)
+    _k3_case(1, 16, 16, path=TEN, act="situ")
 
 
 def test_k3_decode_t256():
