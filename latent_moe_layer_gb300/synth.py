@@ -65,6 +65,7 @@ class LayerConfig:
     act: str = "silu"             # "silu" or "situ" (the GLU activation)
     situ_beta: float = 4.0
     situ_linear_beta: float = 25.0
+    a8: bool = False              # MXFP8 activations into the routed experts (the A8 option)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     def with_tokens(self, T: int) -> "LayerConfig":
@@ -75,6 +76,11 @@ class LayerConfig:
     def with_shared(self, S: int) -> "LayerConfig":
         d = dict(self.__dict__)
         d["S"] = S
+        return LayerConfig(**d)
+
+    def with_a8(self, a8: bool = True) -> "LayerConfig":
+        d = dict(self.__dict__)
+        d["a8"] = a8
         return LayerConfig(**d)
 
     def with_act(self, act: str) -> "LayerConfig":

@@ -44,6 +44,15 @@
  *      soft-limited, and so is the linear (up) branch:
  *        act(g, u) = sigmoid(g) * beta tanh(g/beta) * linear_beta tanh(u/linear_beta).
  *      Parity unpinned beyond the bound and the two limits the pages state.
+ *   6. A8 (optional).  The review's post-training section: from SFT on, the
+ *      routed experts were trained with MXFP4 weights and MXFP8 input
+ *      activations; attention, the latent projections, the shared experts and
+ *      the router keep higher precision.  So the two activation inputs of the
+ *      routed expert GEMMs -- h, and the GLU output a -- are quantised to MXFP8
+ *      per token along the reduction axis: OCP Microscaling v1.0 E4M3 elements
+ *      (round to nearest even, saturating at +-448) with one E8M0 scale per 32,
+ *      X = floor(log2 amax) - 8.  Reading: h is quantised from its BF16 value
+ *      (the precision the layer stores it in), a from its unrounded value.
  *
  * Precision: inputs widen exactly (BF16/fp32 -> fp64); all arithmetic is fp64.
  */
@@ -86,6 +95,54 @@ double oracle_e8m0(unsigned e)
     return ldexp(1.0, (int)e - 127);
 }
 
+/* fp64 -> nearest BF16 value (ties to even), as fp64. */
+double oracle_round_bf16(double v)
+{
+    if (v == 0.0 || !isfinite(v))
+        return v;
+    int e;
+    double m = frexp(v, &e);                     /* v = m 2^e, 0.5 <= |m| < 1 */
+    return ldexp(nearbyint(ldexp(m, 8)), e - 8); /* 8 significant bits */
+}
+
+/* fp64 -> nearest OCP E4M3 value (bias 7, 3 mantissa bits, subnormal spacing
+ * 2^-9, ties to even), saturating at +-448. */
+double oracle_e4m3(double v)
+{
+    double a = fabs(v);
+    if (a == 0.0 || isnan(v))
+        return v;
+    int e = (int)floor(log2(a));
+    if (e < -6)
+        e = -6;                                  /* subnormals: spacing stays 2^-9 */
+    double step = ldexp(1.0, e - 3);
+    double q = nearbyint(a / step) * step;
+    if (q > 448.0)
+        q = 448.0;
+    return v < 0 ? -q : q;
+}
+
+/* One row of n values (n a multiple of 32) -> MXFP8 values: per block of 32,
+ * X = floor(log2 amax) - 8 (kept in [-127, 127]) and E4M3(v / 2^X) 2^X. */
+void oracle_mxfp8_row(const double *in, int n, double *out)
+{
+    for (int b = 0; b < n / 32; b++) {
+        double amax = 0.0;
+        for (int j = 0; j < 32; j++)
+            amax = fmax(amax, fabs(in[32 * b + j]));
+        if (amax == 0.0) {
+            for (int j = 0; j < 32; j++)
+                out[32 * b + j] = 0.0;
+            continue;
+        }
+        int X = (int)floor(log2(amax)) - 8;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+        for (int j = 0; j < 32; j++)
+            out[32 * b + j] = ldexp(oracle_e4m3(ldexp(in[32 * b + j], -X)), X);
+    }
+}
+
 /* Dequantise one row of n MXFP4 values (n a multiple of 32). */
 void oracle_dequant_row(const uint8_t *packed, const uint8_t *scale, int n, double *out)
 {
@@ -112,6 +169,7 @@ typedef struct {
     int has_bias;
     int act;                     /* 0: SiLU; 1: SiTU */
     double situ_beta, situ_linear_beta;
+    int a8;                      /* 1: MXFP8 activations into the routed experts (step 6) */
 } oracle_cfg;
 
 typedef struct {
@@ -218,7 +276,7 @@ void oracle_route(const oracle_cfg *c, const oracle_weights *w, const uint16_t *
  */
 static void glu_apply(const oracle_cfg *c, const uint8_t *w1p, const uint8_t *w1s, const uint8_t *w3p,
                       const uint8_t *w3s, const uint8_t *w2p, const uint8_t *w2s, int din, int dint, int dout,
-                      int ntok, const double *in, const double *coef, double *out)
+                      int ntok, const double *in, const double *coef, double *out, int q8)
 {
     double *a = (double *)malloc(sizeof(double) * (size_t)ntok * dint);
     /* gate/up projections and activation */
@@ -247,6 +305,10 @@ static void glu_apply(const oracle_cfg *c, const uint8_t *w1p, const uint8_t *w1
         free(r1);
         free(r3);
     }
+    /* step 6: the down projection's input in MXFP8 */
+    if (q8)
+        for (int t = 0; t < ntok; t++)
+            oracle_mxfp8_row(a + (size_t)t * dint, dint, a + (size_t)t * dint);
     /* down projection */
 #ifdef _OPENMP
 #pragma omp parallel
@@ -307,6 +369,14 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
                 acc += oracle_bf16(w->w_down[(size_t)r * H + k]) * xin[(size_t)i * H + k];
             h[(size_t)i * L + r] = acc;
         }
+    /* step 6: the routed experts' input h, stored BF16, in MXFP8 */
+    if (c->a8)
+        for (int i = 0; i < n; i++) {
+            double *hr = h + (size_t)i * L;
+            for (int r = 0; r < L; r++)
+                hr[r] = oracle_round_bf16(hr[r]);
+            oracle_mxfp8_row(hr, L, hr);
+        }
 
     /* 3b. experts, expert by expert in index order; z accumulates w_k y_k */
     double *z = (double *)calloc((size_t)n * L, sizeof(double));
@@ -341,7 +411,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
             break;
         memset(y, 0, sizeof(double) * (size_t)m * L);
         glu_apply(c, w->w1p[e], w->w1s[e], w->w3p[e], w->w3s[e], w->w2p[e], w->w2s[e],
-                  L, c->I, L, m, in, coef, y);
+                  L, c->I, L, m, in, coef, y, c->a8);
         for (int q = 0; q < m; q++)
             for (int r = 0; r < L; r++)
                 z[(size_t)members[q] * L + r] += y[(size_t)q * L + r];
@@ -376,7 +446,7 @@ int oracle_forward(const oracle_cfg *c, const oracle_weights *w, const uint16_t 
         double *ones = (double *)malloc(sizeof(double) * n);
         for (int i = 0; i < n; i++)
             ones[i] = 1.0;
-        glu_apply(c, w->ws1p, w->ws1s, w->ws3p, w->ws3s, w->ws2p, w->ws2s, H, c->S, H, n, xin, ones, out);
+        glu_apply(c, w->ws1p, w->ws1s, w->ws3p, w->ws3s, w->ws2p, w->ws2s, H, c->S, H, n, xin, ones, out, 0);
         free(ones);
     }
 

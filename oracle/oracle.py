@@ -35,7 +35,8 @@ class _Cfg(C.Structure):
     _fields_ = [("H", C.c_int), ("L", C.c_int), ("E", C.c_int), ("K", C.c_int),
                 ("I", C.c_int), ("S", C.c_int), ("rms_eps", C.c_double),
                 ("routed_scaling", C.c_double), ("router_bf16", C.c_int), ("has_bias", C.c_int),
-                ("act", C.c_int), ("situ_beta", C.c_double), ("situ_linear_beta", C.c_double)]
+                ("act", C.c_int), ("situ_beta", C.c_double), ("situ_linear_beta", C.c_double),
+                ("a8", C.c_int)]
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -74,6 +75,12 @@ def lib():
             _lib.oracle_max_threads.restype = C.c_int
             _lib.oracle_act.restype = d
             _lib.oracle_act.argtypes = [C.c_int, d, d, d, d]
+            _lib.oracle_round_bf16.restype = d
+            _lib.oracle_round_bf16.argtypes = [d]
+            _lib.oracle_e4m3.restype = d
+            _lib.oracle_e4m3.argtypes = [d]
+            _lib.oracle_mxfp8_row.restype = None
+            _lib.oracle_mxfp8_row.argtypes = [C.c_void_p, C.c_int, C.c_void_p]
     return _lib
 
 
@@ -126,7 +133,8 @@ def _cfg(cfg) -> _Cfg:
     act = {"silu": 0, "situ": 1}[getattr(cfg, "act", "silu")]
     return _Cfg(cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S, cfg.rms_eps, cfg.routed_scaling,
                 1 if cfg.router_dtype == "bf16" else 0, 1 if cfg.select_bias else 0, act,
-                getattr(cfg, "situ_beta", 4.0), getattr(cfg, "situ_linear_beta", 25.0))
+                getattr(cfg, "situ_beta", 4.0), getattr(cfg, "situ_linear_beta", 25.0),
+                1 if getattr(cfg, "a8", False) else 0)
 
 
 def _weights(cfg, dense, experts, keep) -> _W:
@@ -156,6 +164,28 @@ def act(kind: str, g, u, beta: float = 4.0, linear_beta: float = 25.0):
     g, u = np.broadcast_arrays(np.asarray(g, np.float64), np.asarray(u, np.float64))
     return np.array([f(k, beta, linear_beta, float(a), float(b)) for a, b in zip(g.ravel(), u.ravel())]
                     ).reshape(g.shape)
+
+
+def mxfp8(x):
+    """The oracle's MXFP8 rounding (step 6) of the last axis (length a multiple of 32)."""
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.empty_like(x)
+    n = x.shape[-1]
+    for xr, orow in zip(x.reshape(-1, n), out.reshape(-1, n)):
+        lib().oracle_mxfp8_row(xr.ctypes.data, n, orow.ctypes.data)
+    return out
+
+
+def e4m3(v):
+    f = lib().oracle_e4m3
+    v = np.asarray(v, np.float64)
+    return np.array([f(float(a)) for a in v.ravel()]).reshape(v.shape)
+
+
+def round_bf16(v):
+    f = lib().oracle_round_bf16
+    v = np.asarray(v, np.float64)
+    return np.array([f(float(a)) for a in v.ravel()]).reshape(v.shape)
 
 
 def route(cfg, dense, x_rows: np.ndarray, nthreads: int = 0, want_logits: bool = False):

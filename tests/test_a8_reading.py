@@ -1,4 +1,4 @@
-"""The A8 option, measured on the CPU: MXFP8 activations against the exact layer.
+"""The A8 option: pins of the oracle's MXFP8 step, and its cost against the exact layer.
 
 The K3 report review (sections on deployment-aware post-training and on the
 open weights) says the routed experts were trained and are shipped with MXFP4
@@ -91,15 +91,16 @@ def _bf16(bits):
     return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def _layer_from_latent(cfg, dense, experts, h, idx, w, quant):
+def _layer_from_latent(cfg, dense, experts, h, idx, w, quant, quant_h=None):
     """Experts, combine, RMSNorm and up-projection in fp64 from the oracle's latent
-    h, indices and weights; ``quant`` is applied to each expert GEMM's input."""
+    h, indices and weights; ``quant`` is applied to each expert GEMM's input
+    (``quant_h``, when given, to h instead)."""
     up, gamma = _bf16(dense.w_up), _bf16(dense.gamma)
     deq = {e: [oracle.dequant(p, s) for p, s in mats] for e, mats in experts.items()}
     out = np.zeros((h.shape[0], cfg.H))
     for t in range(h.shape[0]):
         z = np.zeros(cfg.L)
-        hq = quant(h[t])
+        hq = (quant_h or quant)(h[t])
         for k in range(cfg.K):
             w1, w3, w2 = deq[int(idx[t, k])]
             g, u = w1 @ hq, w3 @ hq
@@ -133,3 +134,41 @@ def test_mxfp8_activations_exceed_the_parity_bar():
         err = _rel_l2(a8, ref["out"])
         assert 2e-2 < err < 1e-1, (no_clip, err)
         print(f"MXFP8 activations ({'no-clip' if no_clip else 'OCP'} scale): rel-L2 {err:.4f}")
+
+
+# ------------------------------------------------------------------ the oracle's A8 step
+def _bf16_round(v):
+    """Nearest BF16 (ties to even) via float32 bit arithmetic (v exactly representable in fp32)."""
+    f = np.asarray(v, np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16 << 16
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def test_oracle_rounding_steps_match_their_definitions():
+    g = e4m3_grid()
+    assert np.array_equal(oracle.e4m3(g), g) and np.array_equal(oracle.e4m3(-g), -g)
+    r = np.random.default_rng(3).standard_normal(3000) * 10.0 ** np.random.default_rng(4).uniform(-4, 3, 3000)
+    assert np.array_equal(oracle.e4m3(r), e4m3_round(r))
+    assert oracle.e4m3(500.0) == 448.0 and oracle.e4m3(1 + 2 ** -4) == 1.0 and oracle.e4m3(2.0 ** -10) == 0.0
+    x = r[:2048].reshape(4, 512)
+    assert np.array_equal(oracle.mxfp8(x), mxfp8(x))
+    f = r.astype(np.float32).astype(np.float64)
+    assert np.array_equal(oracle.round_bf16(f), _bf16_round(f))
+    assert oracle.round_bf16(1 + 2 ** -8) == 1.0 and oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+
+
+def test_oracle_a8_mode_is_the_restated_layer():
+    # the oracle's A8 option = MXFP8(BF16(h)) into gate/up and MXFP8(a) into down,
+    # re-stated here from the test-local (grid-pinned) rounding
+    cfg = synth.SMALL_ALIGNED.with_tokens(8)
+    dense = synth.gen_dense(cfg)
+    x = synth.gen_x(cfg)
+    idx, _, _, _ = oracle.route(cfg, dense, x)
+    experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+    exact = oracle.forward(cfg, dense, experts, x, want_latent=True)
+    a8 = oracle.forward(cfg.with_a8(), dense, experts, x)
+    re = _layer_from_latent(cfg, dense, experts, exact["h"], exact["idx"], exact["w"], mxfp8,
+                            quant_h=lambda v: mxfp8(_bf16_round(v)))
+    assert _rel_l2(a8["out"], re) < 1e-12
+    assert 2e-2 < _rel_l2(a8["out"], exact["out"]) < 1e-1
