@@ -53,6 +53,8 @@ def workload_name(cfg):
         s += ", Zipf(1.1) selection bias"
     if getattr(cfg, "act", "silu") != "silu":
         s += f", {cfg.act} GLU"
+    if getattr(cfg, "a8", False):
+        s += ", MXFP8 activations into the routed experts"
     return s
 
 
@@ -232,6 +234,8 @@ def run_ours(args):
         cfg = synth.LayerConfig(**{**cfg.__dict__, "T": args.tokens, "name": cfg.name + f"_T{args.tokens}"})
     if args.act != "silu":
         cfg = synth.LayerConfig(**{**cfg.__dict__, "act": args.act, "name": cfg.name + f"_{args.act}"})
+    if args.a8:
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "a8": True, "name": cfg.name + "_a8"})
     pk, pk_src = peaks()
 
     dw = k3moe.DeviceWeights(cfg)
@@ -500,6 +504,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling aid)")
     ap.add_argument("--act", default="silu", choices=["silu", "situ"],
                     help="GLU activation (the workload's is SiLU; SiTU is the option the layer also supports)")
+    ap.add_argument("--a8", action="store_true", help="MXFP8 activations into the routed experts (the A8 option)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--library-peaks", action="store_true",

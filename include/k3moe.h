@@ -92,7 +92,20 @@ typedef struct k3moe_config {
     int path;            /* K3MOE_PATH_* */
     float situ_beta;        /* K3MOE_ACT_SITU gate-branch beta (<= 0: 4.0) */
     float situ_linear_beta; /* K3MOE_ACT_SITU up-branch beta (<= 0: 25.0) */
+    int a8;                 /* 1: MXFP8 activations into the routed experts (K3MOE_A8 below) */
 } k3moe_config;
+
+/*
+ * A8 option (a8 = 1).  The K3 report review's post-training passage: the routed
+ * experts were trained and are shipped with MXFP4 weights and MXFP8 input
+ * activations, while attention, the latent projections, the shared experts and
+ * the router keep higher precision.  With a8 set, the two activation inputs of
+ * the routed expert GEMMs are rounded to OCP MXFP8 per token along K -- E4M3
+ * elements (nearest even, saturating at +-448) with one E8M0 scale per 32
+ * values, scale = 2^(floor(log2 amax) - 8): the latent h from its BF16 value,
+ * and the GLU output from its fp32 value.  The GEMMs themselves are unchanged
+ * (exact on these values); the shared experts stay A16.
+ */
 
 /*
  * Weights, all device pointers, borrowed from load_weights until destroy.

@@ -115,6 +115,7 @@ int k3moe_create(const k3moe_config *cfg, k3moe_handle **out)
     if (c.latent > 8192) return K3MOE_ERR_SHAPE;
     if (c.act != K3MOE_ACT_SILU && c.act != K3MOE_ACT_SITU) return K3MOE_ERR_UNSUPPORTED;
     if (!(c.situ_beta == c.situ_beta) || !(c.situ_linear_beta == c.situ_linear_beta)) return K3MOE_ERR_ARG;
+    if (c.a8 != 0 && c.a8 != 1) return K3MOE_ERR_ARG;
     if (c.router_dtype != K3MOE_ROUTER_F32 && c.router_dtype != K3MOE_ROUTER_BF16) return K3MOE_ERR_ARG;
     if (c.path < K3MOE_PATH_AUTO || c.path > K3MOE_PATH_TENSOR) return K3MOE_ERR_ARG;
     if (!(c.rms_eps >= 0.f) || !(c.routed_scaling == c.routed_scaling)) return K3MOE_ERR_ARG;
@@ -319,7 +320,8 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->tiles = cv.take<int32_t>(4 * (R + c.n_experts + 1));
     ws->act = cv.take<float>(R * c.inter + 1);          // fp32 (generic) or f16 (tensor)
     ws->y = cv.take<float>(R * c.latent + 1);
-    ws->hperm = cv.take<uint16_t>(R * c.latent + 1);
+    // f16 expert inputs: the permuted h; with A8 also the MXFP8 GLU output [R, I]
+    ws->hperm = cv.take<uint16_t>(R * (c.latent > c.inter ? c.latent : c.inter) + 1);
     ws->hscale = cv.take<float>(R + 1);
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
     ws->o32 = cv.take<float>(Tn * c.hidden);
@@ -359,6 +361,9 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
     {   // latent h (BF16)
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
         if ((rc = k3_launch_rows_gemm(x, 1, T, H, h->w_down, 1, L, nullptr, ws.h, 0, st))) return rc;
+        // A8: the routed experts read h as MXFP8
+        if (c.a8 && (rc = k3_launch_mx8_rows(ws.h, 0, ws.h, 0, (size_t)T * L, h->d_status, h->num_sms, st)))
+            return rc;
     }
     if ((rc = k3_launch_route(h, ws, T, 0, st))) return rc;   // top-K and the permutation
     {
@@ -366,6 +371,9 @@ static int forward_generic(k3moe_handle *h, const void *x, int T, void *out, con
         if ((rc = k3_launch_glu_generic(k3_act_of(h->cfg), ws.h, L, ws.tok_of, R, h->d_eptr[0], h->d_eptr[1], h->d_eptr[2],
                                         h->d_eptr[3], ws.offsets, E, I, (float *)ws.act, h->d_status,
                                         st)))
+            return rc;
+        // A8: the down projection reads the GLU output as MXFP8
+        if (c.a8 && (rc = k3_launch_mx8_rows(ws.act, 1, ws.act, 1, (size_t)R * I, h->d_status, h->num_sms, st)))
             return rc;
     }
     {

@@ -246,8 +246,12 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                             const float gv = acc[0][nb][q] * rs;
                             const float uv = acc[NMAT - 1][nb][q] * rs;
                             const float av = k3_glu(gv, uv, a.act);
-                            if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
-                            reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
+                            if (a.out_f32) {
+                                reinterpret_cast<float *>(a.out)[orow * a.rows + row] = av;
+                            } else {
+                                if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
+                                reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
+                            }
                         } else {
                             reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] =
                                 f32_to_bf16(acc[0][nb][q]);

@@ -18,7 +18,8 @@ struct GemvArgs {
     const int *n_tiles;                // device count of tiles
     const float *rscale;               // [R] per-row factor applied to the GLU inputs, or nullptr
     K3Act act;                         // GLU activation
-    void *out;                         // GLU: f16 [R, rows]; BF16: BF16 [R, rows]
+    int out_f32;                       // GLU: 1 writes fp32 [R, rows] (the A8 path rounds it afterwards)
+    void *out;                         // GLU: f16 (or fp32) [R, rows]; BF16: BF16 [R, rows]
     int *status;
 };
 

@@ -8,6 +8,8 @@
 // MXFP4 decoding: "Kimi K3, as released", Gate 3 section (two E2M1 codes per
 // byte, low nibble first; one E8M0 exponent per 32 weights, value 2^(e-127)).
 #include "k3moe_internal.h"
+
+#include <algorithm>
 #include "ptx.cuh"
 
 namespace k3 {
@@ -381,6 +383,53 @@ __global__ void wait_debug_kernel(int *status, int spin_limit)
     }
 }
 
+// ---- A8: OCP MXFP8 rounding of activation rows (blocks of 32 along a row).
+// One warp per block: lane j holds element j; X = floor(log2 amax) - 8 from the
+// exponent field of amax (kept >= -127); each value becomes E4M3(v / 2^X) 2^X
+// with the hardware's round-to-nearest-even, saturating E4M3 conversion.
+template <typename T> __device__ __forceinline__ float mx8_load(const T *p);
+template <> __device__ __forceinline__ float mx8_load<uint16_t>(const uint16_t *p) { return bf16_to_f32(*p); }
+template <> __device__ __forceinline__ float mx8_load<float>(const float *p) { return *p; }
+
+__device__ __forceinline__ float e4m3_rne_sat(float v)
+{
+    uint16_t p;
+    uint32_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p) : "f"(v), "f"(v));   // both bytes: no order question
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(p));
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// out_kind: 0 BF16, 1 fp32, 2 f16 (|q| > 65504 is reported as K3MOE_ERR_RANGE)
+template <typename TI>
+__global__ void __launch_bounds__(256) mx8_rows_kernel(const TI *__restrict__ in, void *__restrict__ out,
+                                                       int out_kind, size_t nblk, int *status)
+{
+    griddep_enter();
+    const int lane = threadIdx.x & 31;
+    const size_t w0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+    for (size_t b = w0; b < nblk; b += nw) {
+        const size_t i = b * 32 + lane;
+        const float v = mx8_load<TI>(in + i);
+        float amax = fabsf(v);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+        const int X = max(ef - 127 - 8, -127);
+        // 2^-X and 2^X as fp32 (2^-127 is the subnormal 0x00400000)
+        const float down = __uint_as_float((uint32_t)(127 - X) << 23);
+        const float up = X > -127 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
+        const float q = amax > 0.f ? e4m3_rne_sat(v * down) * up : 0.f;
+        if (out_kind == 0) reinterpret_cast<uint16_t *>(out)[i] = f32_to_bf16(q);
+        else if (out_kind == 1) reinterpret_cast<float *>(out)[i] = q;
+        else {
+            if (!(fabsf(q) <= 65504.f)) set_status(status, K3MOE_ERR_RANGE, 4);
+            reinterpret_cast<__half *>(out)[i] = __float2half_rn(q);
+        }
+    }
+}
+
 }  // namespace k3
 
 using namespace k3;
@@ -465,6 +514,21 @@ int k3_launch_dequant_debug(const uint8_t *packed, const uint8_t *scale, int row
 int k3_launch_wait_debug(int *status, int spin_limit, cudaStream_t st)
 {
     wait_debug_kernel<<<1, 32, 0, st>>>(status, spin_limit < 1 ? 1 : spin_limit);
+    k3_note_launch();
+    return K3_LAUNCH_OK();
+}
+
+int k3_launch_mx8_rows(const void *in, int in_fp32, void *out, int out_kind, size_t n, int *status, int num_sms,
+                       cudaStream_t st)
+{
+    if (n == 0) return K3MOE_OK;
+    if (n % 32) return K3MOE_ERR_SHAPE;
+    const size_t nblk = n / 32;
+    const unsigned grid = (unsigned)std::min<size_t>((nblk + 7) / 8, (size_t)8 * (num_sms > 0 ? num_sms : 148));
+    if (in_fp32)
+        k3_launch(mx8_rows_kernel<float>, grid, 256, 0, st, (const float *)in, out, out_kind, nblk, status);
+    else
+        k3_launch(mx8_rows_kernel<uint16_t>, grid, 256, 0, st, (const uint16_t *)in, out, out_kind, nblk, status);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }

@@ -256,6 +256,11 @@ int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStr
 // generic CUDA-core kernels (generic.cu)
 int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,
                         float *out_f32, uint16_t *out_bf16, int accumulate, cudaStream_t st);
+// A8: n values (n a multiple of 32; blocks of 32 along rows) rounded to OCP MXFP8;
+// in BF16 (in_fp32 = 0) or fp32; out_kind 0 BF16, 1 fp32, 2 f16.  in may equal out
+// when the element sizes match.
+int k3_launch_mx8_rows(const void *in, int in_fp32, void *out, int out_kind, size_t n, int *status, int num_sms,
+                       cudaStream_t st);
 int k3_launch_glu_generic(const k3::K3Act &act_fn, const uint16_t *in, int din, const int32_t *row_token, int rows,
                           const uint8_t *const *w1p, const uint8_t *const *w1s,
                           const uint8_t *const *w3p, const uint8_t *const *w3s,

@@ -406,7 +406,8 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 // shared memory goes to activation slots.
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
-                       cudaStream_t st, int stage1, int stage2, bool add)
+                       cudaStream_t st, int stage1, int stage2, bool add, size_t mx8_n = 0,
+                       void *mx8_out = nullptr)
 {
     int rc;
     const int ns = h->num_sms;
@@ -416,6 +417,8 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
              : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true>(b1, a1, max_tiles1, ns, st)
                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
+        // A8: the GLU output (fp32) rounded to MXFP8, as the down projection's f16 input
+        if (mx8_n && (rc = k3_launch_mx8_rows(a1.out, 1, mx8_out, 2, mx8_n, a1.status, ns, st))) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
@@ -440,6 +443,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     const int bn = pick_bn(T, K, E);
     int rc;
     if ((rc = dense_router_down(h, x, T, ws, st))) return rc;
+    // A8: the routed experts read h as MXFP8 (rounded in place from its BF16 value)
+    if (c.a8 && (rc = k3_launch_mx8_rows(ws.h, 0, ws.h, 0, (size_t)T * L, h->d_status, h->num_sms, st)))
+        return rc;
     const bool gemv = bn == 32;     // routed experts at decode sizes: the streaming GEMV
     // top-K and the permutation; token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
     if ((rc = k3_launch_route(h, ws, T, gemv ? 16 : bn, st))) return rc;
@@ -452,7 +458,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
     ActMaps bm1, bm2;
-    if (!encode_act_maps(&bm1, ws.hperm, R, L) || !encode_act_maps(&bm2, ws.act, R, I)) return K3MOE_ERR_CUDA;
+    // the down projection's f16 input: the GLU output, or with A8 its MXFP8 rounding (in hperm)
+    void *act16 = c.a8 ? (void *)ws.hperm : (void *)ws.act;
+    if (!encode_act_maps(&bm1, ws.hperm, R, L) || !encode_act_maps(&bm2, act16, R, I)) return K3MOE_ERR_CUDA;
     const uint8_t *rm = h->d_rowmax;
     ExpertGemmArgs a1 = {};
     a1.amaps = (const CUtensorMap *)h->d_tmaps;
@@ -470,9 +478,11 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a1.rscale = ws.hscale;
     a1.act = k3_act_of(c);
     a1.out = ws.act;
+    a1.out_f32 = c.a8;
     a1.status = h->d_status;
     a1.spin_limit = 0xFFFFFFFFu;
     ExpertGemmArgs a2 = a1;
+    a2.out_f32 = 0;
     a2.amap_off[0] = a2.amap_off[1] = 2;
     a2.scales[0] = a2.scales[1] = h->d_eptr[5];
     a2.rowmax[0] = a2.rowmax[1] = rm + (size_t)2 * E * I;
@@ -496,8 +506,10 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g1.rscale = ws.hscale;
         g1.act = k3_act_of(c);
         g1.out = ws.act;
+        g1.out_f32 = c.a8;
         g1.status = h->d_status;
         GemvArgs g2 = g1;
+        g2.out_f32 = 0;
         g2.amap_off[0] = g2.amap_off[1] = 2;
         g2.scales[0] = g2.scales[1] = h->d_eptr[5];
         g2.rows = L;
@@ -510,16 +522,21 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
             if (!encode_act(&gb1, ws.hperm, R, L, 16)) return K3MOE_ERR_CUDA;
             if ((rc = k3_launch_gemv_expert(1, GV_GLU_F16, gb1, g1, max_ntiles * (I / 128), h->num_sms, st)))
                 return rc;
+            // A8: the GLU output (fp32) rounded to MXFP8, as the down projection's f16 input
+            if (c.a8 && (rc = k3_launch_mx8_rows(ws.act, 1, ws.hperm, 2, (size_t)R * I, h->d_status, h->num_sms,
+                                                 st)))
+                return rc;
         }
         {
             k3_stage sg(h, K3MOE_STAGE_EXPERT_DOWN, st);
             CUtensorMap gb2;
-            if (!encode_act(&gb2, ws.act, R, I, 16)) return K3MOE_ERR_CUDA;
+            if (!encode_act(&gb2, act16, R, I, 16)) return K3MOE_ERR_CUDA;
             if ((rc = k3_launch_gemv_expert(0, GV_BF16, gb2, g2, max_ntiles * (L / 128), h->num_sms, st)))
                 return rc;
         }
     } else if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM),
-                                 st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false))) {
+                                 st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false,
+                                 c.a8 ? (size_t)R * I : 0, ws.hperm))) {
         return rc;
     }
     {
@@ -548,6 +565,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         if (!encode_act_maps(&sb1, ws.xs, T, H) || !encode_act_maps(&sb2, ws.sact, T, S)) return K3MOE_ERR_CUDA;
         const uint8_t *rs = rm + (size_t)E * (2 * I + L);
         ExpertGemmArgs s1 = a1;
+        s1.out_f32 = 0;                              // the shared experts stay A16
         s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;
         s1.amap_stride = 3;
         s1.scales[0] = k3_shared_tab(h, 1);

@@ -50,6 +50,7 @@ struct ExpertGemmArgs {
     int *status;
     uint32_t spin_limit;
     K3Act act;                       // GLU activation
+    int out_f32;                     // GLU: 1 writes fp32 [R, rows] (the A8 path rounds it afterwards)
 };
 
 constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
@@ -485,14 +486,20 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                             const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                             float a;
-                            if (situ)
+                            if (args.out_f32)        // A8: its MXFP8 rounding needs the accurate value
+                                a = k3_glu(2.0f * hv, uv, args.act);
+                            else if (situ)
                                 a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
                                     tanh_approx(hv * (2.0f * args.act.inv_beta)) *
                                     (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
                             else
                                 a = fmaf(hv, tanh_approx(hv), hv) * uv;
-                            bad |= !(fabsf(a) <= 65504.f);
-                            reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
+                            if (args.out_f32) {
+                                reinterpret_cast<float *>(args.out)[orow * args.rows + row] = a;
+                            } else {
+                                bad |= !(fabsf(a) <= 65504.f);
+                                reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
+                            }
                         } else if (MODE == OUT_BF16) {
                             uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
                             o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);

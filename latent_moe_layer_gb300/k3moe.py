@@ -42,7 +42,7 @@ class Config(C.Structure):
                 ("inter", C.c_int), ("shared_inter", C.c_int), ("rms_eps", C.c_float),
                 ("routed_scaling", C.c_float), ("act", C.c_int), ("router_dtype", C.c_int),
                 ("has_select_bias", C.c_int), ("path", C.c_int), ("situ_beta", C.c_float),
-                ("situ_linear_beta", C.c_float)]
+                ("situ_linear_beta", C.c_float), ("a8", C.c_int)]
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -119,7 +119,7 @@ def make_config(cfg, path=PATH_AUTO) -> Config:
     return Config(cfg.H, cfg.L, cfg.E, cfg.K, cfg.I, cfg.S, cfg.rms_eps, cfg.routed_scaling, act,
                   ROUTER_BF16 if cfg.router_dtype == "bf16" else ROUTER_F32,
                   1 if cfg.select_bias else 0, path, getattr(cfg, "situ_beta", 4.0),
-                  getattr(cfg, "situ_linear_beta", 25.0))
+                  getattr(cfg, "situ_linear_beta", 25.0), 1 if getattr(cfg, "a8", False) else 0)
 
 
 class Layer:

@@ -72,6 +72,7 @@ def compare(cfg, gpu, ref, rows=None):
     rel = float(np.linalg.norm(err) / np.linalg.norm(r_out))
     rms = float(np.sqrt((r_out ** 2).mean()))
     mx = float(np.abs(err).max() / max(rms, 1.0))
+    over = int((np.abs(err) / max(rms, 1.0) > MAX_ABS).sum())
     sel = ref["gap"] >= GAP
     near = int((~sel).sum())
     idx_bad = [int(t) for t in np.nonzero(sel)[0]
@@ -85,7 +86,7 @@ def compare(cfg, gpu, ref, rows=None):
         for k, e in enumerate(g_idx[t]):
             w_err = max(w_err, abs(g_w[t, k] - ref["w"][t, pos[int(e)]]))
     return dict(rel_l2=rel, max_abs=mx, near_ties=near, idx_mismatch=len(idx_bad),
-                w_err=w_err, out_rms=rms, order_bad=order_bad)
+                w_err=w_err, out_rms=rms, order_bad=order_bad, over_max_abs=over, n_out=int(err.size))
 
 
 def assert_parity(m):
