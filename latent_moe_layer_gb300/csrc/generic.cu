@@ -391,14 +391,6 @@ template <typename T> __device__ __forceinline__ float mx8_load(const T *p);
 template <> __device__ __forceinline__ float mx8_load<uint16_t>(const uint16_t *p) { return bf16_to_f32(*p); }
 template <> __device__ __forceinline__ float mx8_load<float>(const float *p) { return *p; }
 
-__device__ __forceinline__ float e4m3_rne_sat(float v)
-{
-    uint16_t p;
-    uint32_t h;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p) : "f"(v), "f"(v));   // both bytes: no order question
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(p));
-    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-}
 
 // out_kind: 0 BF16, 1 fp32, 2 f16 (|q| > 65504 is reported as K3MOE_ERR_RANGE)
 template <typename TI>
@@ -415,12 +407,7 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const TI *__restrict__ in
         float amax = fabsf(v);
 #pragma unroll
         for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-        const int X = max(ef - 127 - 8, -127);
-        // 2^-X and 2^X as fp32 (2^-127 is the subnormal 0x00400000)
-        const float down = __uint_as_float((uint32_t)(127 - X) << 23);
-        const float up = X > -127 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
-        const float q = amax > 0.f ? e4m3_rne_sat(v * down) * up : 0.f;
+        const float q = mx8_round(v, amax);
         if (out_kind == 0) reinterpret_cast<uint16_t *>(out)[i] = f32_to_bf16(q);
         else if (out_kind == 1) reinterpret_cast<float *>(out)[i] = q;
         else {

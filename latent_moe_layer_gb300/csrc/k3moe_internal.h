@@ -60,6 +60,36 @@ __device__ __forceinline__ float k3_glu(float g, float u, const K3Act &a)
     return g * sg * u;
 }
 
+// OCP E4M3 rounding of v (nearest even, saturating at +-448) with the hardware conversion.
+__device__ __forceinline__ float e4m3_rne_sat(float v)
+{
+    uint16_t p;
+    uint32_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p) : "f"(v), "f"(v));   // both bytes: no order question
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(p));
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// MXFP8 value of v in a block of 32 whose largest magnitude is amax (OCP MX v1.0):
+// scale 2^X with X = floor(log2 amax) - 8 (from amax's exponent field, kept >= -127),
+// element E4M3(v / 2^X).
+// The same from the block scale exponent X (-127 <= X <= 119).
+__device__ __forceinline__ float mx8_round_x(float v, int X)
+{
+    const float down = __uint_as_float((uint32_t)(127 - X) << 23);     // 2^-X (X >= -127: at most 2^127)
+    const float up = X > -127 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
+    return e4m3_rne_sat(v * down) * up;
+}
+
+// X from the block's largest exponent field (floor(log2 amax) = field - 127 for
+// normal amax; zero and subnormal blocks take the clamp, -127).
+__device__ __forceinline__ int mx8_scale_exp(uint32_t max_exp_field) { return max((int)max_exp_field - 135, -127); }
+
+__device__ __forceinline__ float mx8_round(float v, float amax)
+{
+    return mx8_round_x(v, mx8_scale_exp((__float_as_uint(amax) >> 23) & 0xFF));
+}
+
 // 2^(e-127) for an E8M0 byte e in [0, 254] (e = 0 gives the fp32 subnormal 2^-127).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e)
 {

@@ -406,8 +406,7 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 // shared memory goes to activation slots.
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
-                       cudaStream_t st, int stage1, int stage2, bool add, size_t mx8_n = 0,
-                       void *mx8_out = nullptr)
+                       cudaStream_t st, int stage1, int stage2, bool add)
 {
     int rc;
     const int ns = h->num_sms;
@@ -417,8 +416,6 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
              : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true>(b1, a1, max_tiles1, ns, st)
                          : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
-        // A8: the GLU output (fp32) rounded to MXFP8, as the down projection's f16 input
-        if (mx8_n && (rc = k3_launch_mx8_rows(a1.out, 1, mx8_out, 2, mx8_n, a1.status, ns, st))) return rc;
     }
     {
         k3_stage sg(h, stage2, st);
@@ -458,8 +455,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
     ActMaps bm1, bm2;
-    // the down projection's f16 input: the GLU output, or with A8 its MXFP8 rounding (in hperm)
-    void *act16 = c.a8 ? (void *)ws.hperm : (void *)ws.act;
+    // the down projection's f16 input: the GLU output (MXFP8-rounded in the tcgen05 epilogue
+    // with A8), or for the decode GEMV with A8 its rounding from fp32 (in hperm)
+    void *act16 = (c.a8 && gemv) ? (void *)ws.hperm : (void *)ws.act;
     if (!encode_act_maps(&bm1, ws.hperm, R, L) || !encode_act_maps(&bm2, act16, R, I)) return K3MOE_ERR_CUDA;
     const uint8_t *rm = h->d_rowmax;
     ExpertGemmArgs a1 = {};
@@ -478,11 +476,11 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a1.rscale = ws.hscale;
     a1.act = k3_act_of(c);
     a1.out = ws.act;
-    a1.out_f32 = c.a8;
+    a1.a8 = c.a8;                                // MXFP8 rounding fused in the GLU epilogue
     a1.status = h->d_status;
     a1.spin_limit = 0xFFFFFFFFu;
     ExpertGemmArgs a2 = a1;
-    a2.out_f32 = 0;
+    a2.a8 = 0;
     a2.amap_off[0] = a2.amap_off[1] = 2;
     a2.scales[0] = a2.scales[1] = h->d_eptr[5];
     a2.rowmax[0] = a2.rowmax[1] = rm + (size_t)2 * E * I;
@@ -535,8 +533,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
                 return rc;
         }
     } else if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM),
-                                 st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false,
-                                 c.a8 ? (size_t)R * I : 0, ws.hperm))) {
+                                 st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false))) {
         return rc;
     }
     {
@@ -565,7 +562,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         if (!encode_act_maps(&sb1, ws.xs, T, H) || !encode_act_maps(&sb2, ws.sact, T, S)) return K3MOE_ERR_CUDA;
         const uint8_t *rs = rm + (size_t)E * (2 * I + L);
         ExpertGemmArgs s1 = a1;
-        s1.out_f32 = 0;                              // the shared experts stay A16
+        s1.a8 = 0;                                   // the shared experts stay A16
         s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;
         s1.amap_stride = 3;
         s1.scales[0] = k3_shared_tab(h, 1);

@@ -50,7 +50,7 @@ struct ExpertGemmArgs {
     int *status;
     uint32_t spin_limit;
     K3Act act;                       // GLU activation
-    int out_f32;                     // GLU: 1 writes fp32 [R, rows] (the A8 path rounds it afterwards)
+    int a8;                          // GLU: 1 rounds the output to MXFP8 (blocks of 32 rows per token)
 };
 
 constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
@@ -473,6 +473,42 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
                 tc_wait_ld();
+                if (MODE == OUT_GLU_F16 && args.a8) {
+                    // A8: the accurate activation, rounded to MXFP8 over the 32 consecutive
+                    // weight rows this warp's lanes hold (one block of the down projection's K
+                    // for each token): the 16 tokens' largest exponent fields, packed four to a
+                    // word, are reduced over the lanes with byte-wise maxima
+                    float av[16];
+                    uint32_t pk[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c * 16 + j;
+                        float a = 0.f;
+                        if (n < nrows) {
+                            const float rs = srs[n];
+                            const float gv = __uint_as_float(v0[j]) * (fw0 * rs);
+                            const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
+                            a = situ ? k3_glu(gv, uv, args.act) : __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                        }
+                        av[j] = a;
+                        pk[j >> 2] |= ((__float_as_uint(a) >> 23) & 0xFFu) << (8 * (j & 3));
+                    }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) pk[w] = __vmaxu4(pk[w], __shfl_xor_sync(0xffffffffu, pk[w], o));
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c * 16 + j;
+                        if (n < nrows) {
+                            const float a = mx8_round_x(av[j], mx8_scale_exp((pk[j >> 2] >> (8 * (j & 3))) & 0xFFu));
+                            bad |= !(fabsf(a) <= 65504.f);
+                            reinterpret_cast<__half *>(args.out)[(size_t)(row0 + n) * args.rows + row] =
+                                __float2half_rn(a);
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c * 16 + j;
@@ -486,20 +522,14 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                             const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                             float a;
-                            if (args.out_f32)        // A8: its MXFP8 rounding needs the accurate value
-                                a = k3_glu(2.0f * hv, uv, args.act);
-                            else if (situ)
+                            if (situ)
                                 a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
                                     tanh_approx(hv * (2.0f * args.act.inv_beta)) *
                                     (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
                             else
                                 a = fmaf(hv, tanh_approx(hv), hv) * uv;
-                            if (args.out_f32) {
-                                reinterpret_cast<float *>(args.out)[orow * args.rows + row] = a;
-                            } else {
-                                bad |= !(fabsf(a) <= 65504.f);
-                                reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
-                            }
+                            bad |= !(fabsf(a) <= 65504.f);
+                            reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                         } else if (MODE == OUT_BF16) {
                             uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
                             o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
