@@ -40,6 +40,15 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t (&o)[4])
         : "r"(w));
 }
 
+// ldmatrix of 8x8 b16 tiles: lane t receives bytes [4 (t % 4), +4) of row t / 4 of
+// each tile; lanes 8i .. 8i + 7 give the row addresses of tile i.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
 // 2^(e - 127) for the E8M0 byte `e`, exact in fp32 (e = 0 is taken as 0).
 __device__ __forceinline__ float e8m0_f32_noden(uint32_t e) { return __uint_as_float(e << 23); }
 
@@ -69,7 +78,6 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                                             uint32_t &it, float (&acc)[NMAT][2][4])
 {
     using SM = GvSmem<NMAT, NS>;
-    const int rb_l = ra_l + 8;
     // scale bytes: 8 per row and stage (blocks 8s .. 8s+7), read one stage ahead
     uint2 sca[NMAT], scb[NMAT], nsa[NMAT], nsb[NMAT];
 #pragma unroll
@@ -91,6 +99,10 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
         if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, 0xFFFFFFFFu, a.status, 12)) return false;
         const uint8_t *sbase = smem + slot * SM::STAGE;
         const uint8_t *bbase = sbase + NMAT * GV_STAGE_BYTES;
+        // ldmatrix row base of this lane: tile (lane >> 3) = (matrix, rows ra or rb)
+        const int cw_rows = ra_l >> 4;                   // this warp's 16-row group
+        const uint32_t sld = smem_u32(sbase) + ((lane >> 4) & (NMAT - 1)) * GV_STAGE_BYTES +
+                             (16 * cw_rows + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
@@ -98,12 +110,16 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                 // MX block j = 2 ks + bl of the stage = 16-byte chunk j of each 128-byte row;
                 // this thread takes bytes [4c, 4c + 4) of it
                 const int j = 2 * ks + bl;
+                // gate/up: one ldmatrix for tiles (rows ra, matrix 0), (rows rb, 0), (ra, 1),
+                // (rb, 1), this lane's row address being row (lane & 7) of its tile, chunk j
+                // (128-byte swizzle); down: two plain loads (measured faster than ldmatrix.x2)
                 uint32_t pa[NMAT], pb[NMAT];
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    const uint8_t *base = sbase + m * GV_STAGE_BYTES;
-                    pa[m] = *reinterpret_cast<const uint32_t *>(base + ra_l * 128 + 16 * (j ^ g8) + 4 * c);
-                    pb[m] = *reinterpret_cast<const uint32_t *>(base + rb_l * 128 + 16 * (j ^ g8) + 4 * c);
+                if (NMAT == 2) {
+                    ldsm_x4(sld + 16 * (j ^ (lane & 7)), pa[0], pb[0], pa[NMAT - 1], pb[NMAT - 1]);
+                } else {
+                    const uint8_t *base = sbase + 16 * cw_rows * 128 + 16 * (j ^ g8) + 4 * c;
+                    pa[0] = *reinterpret_cast<const uint32_t *>(base + g8 * 128);
+                    pb[0] = *reinterpret_cast<const uint32_t *>(base + (g8 + 8) * 128);
                 }
                 // token 8 nb + g8 at block-local K = 8c .. 8c + 7: 16-byte chunk 4 bl + c of its
                 // row in box ks (128-byte swizzle)
