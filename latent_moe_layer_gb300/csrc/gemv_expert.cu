@@ -49,6 +49,9 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
                  : "r"(addr));
 }
 
+// Token row of B (within an 8-token block) that MMA column n reads: 0, 4, 1, 5, 2, 6, 3, 7.
+__device__ __forceinline__ int tok_perm(int n) { return (n >> 1) | ((n & 1) << 2); }
+
 // 2^(e - 127) for the E8M0 byte `e`, exact in fp32 (e = 0 is taken as 0).
 __device__ __forceinline__ float e8m0_f32_noden(uint32_t e) { return __uint_as_float(e << 23); }
 
@@ -77,6 +80,7 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                                             int g8, int c, int lane, const uint2 *const (&sa)[NMAT], int rbo,
                                             uint32_t &it, float (&acc)[NMAT][2][4])
 {
+    const int tr = tok_perm(g8);
     using SM = GvSmem<NMAT, NS>;
     // scale bytes: 8 per row and stage (blocks 8s .. 8s+7), read one stage ahead
     uint2 sca[NMAT], scb[NMAT], nsa[NMAT], nsb[NMAT];
@@ -121,13 +125,15 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                     pa[0] = *reinterpret_cast<const uint32_t *>(base + g8 * 128);
                     pb[0] = *reinterpret_cast<const uint32_t *>(base + (g8 + 8) * 128);
                 }
-                // token 8 nb + g8 at block-local K = 8c .. 8c + 7: 16-byte chunk 4 bl + c of its
-                // row in box ks (128-byte swizzle)
+                // MMA column g8 takes token row 8 nb + tr (tr = tok_perm(g8)) at block-local
+                // K = 8c .. 8c + 7: 16-byte chunk 4 bl + c of that row in box ks (128-byte
+                // swizzle).  The two rows a quarter-warp reads differ by 4, so their chunks
+                // fall in disjoint bank groups
                 uint4 hb[NNB];
 #pragma unroll
                 for (int nb = 0; nb < NNB; ++nb)
-                    hb[nb] = *reinterpret_cast<const uint4 *>(bbase + ks * 16 * 128 + (8 * nb + g8) * 128 +
-                                                              16 * ((4 * bl + c) ^ g8));
+                    hb[nb] = *reinterpret_cast<const uint4 *>(bbase + ks * 16 * 128 + (8 * nb + tr) * 128 +
+                                                              16 * ((4 * bl + c) ^ tr));
                 if (ks == 3 && bl == 1) {
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
             for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int tok = 8 * nb + 2 * c + (q & 1);
+                    const int tok = 8 * nb + tok_perm(2 * c + (q & 1));
                     const int row = (q < 2) ? ra : rb;
                     if (tok < nt) {
                         const size_t orow = (size_t)(b_first + tok);
