@@ -154,12 +154,12 @@ __global__ void dense_tiles_kernel(int T, int bn, int4 *tiles, int32_t *count)
     if (threadIdx.x == 0) *count = n;
 }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false, int EPI = EPI_SILU>
 int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, int num_sms, cudaStream_t st)
 {
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
     static_assert(SM::BYTES <= 227 * 1024, "shared memory");
-    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE, ATMEM>;
+    auto kern = expert_gemm_kernel<NMAT, BN, NS, NB, NA, NACC, MODE, ATMEM, EPI>;
     static unsigned long long attr_set = 0;
     if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int grid = max(1, min(num_sms, max_tiles));
@@ -315,7 +315,6 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
         !k3_encode_bf16_rows(&br, hilo ? (const void *)h->d_router_hilo : h->w_router, E, hilo ? 2 * H : H, bn) ||
         !k3_encode_bf16_rows(&bd, h->w_down, L, H, bn))
         return K3MOE_ERR_CUDA;
-    const int mt = (T + 127) / 128;
     DenseArgs a = {};
     a.nseg = 2;
     a.M = T;
@@ -373,7 +372,6 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     CUtensorMap an, bu;
     if (!k3_encode_bf16_rows(&an, ws.nrm, T, L, 128) || !k3_encode_bf16_rows(&bu, h->w_up, H, L, bn))
         return K3MOE_ERR_CUDA;
-    const int mt = (T + 127) / 128;
     DenseArgs a = {};
     a.nseg = 1;
     a.M = T;
@@ -404,6 +402,15 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 // 256 weight rows per job (two 128-row blocks against one activation tile,
 // halving activation traffic).  Activation loads are latency-bound, so spare
 // shared memory goes to activation slots.
+// The gate/up GEMM of tile shape bn with GLU variant EPI.
+template <int EPI>
+static int launch_glu(int bn, const ActMaps &b1, const ExpertGemmArgs &a1, int max_tiles1, int ns, cudaStream_t st)
+{
+    return bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16, false, EPI>(b1, a1, max_tiles1, ns, st)
+           : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true, EPI>(b1, a1, max_tiles1, ns, st)
+                       : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16, false, EPI>(b1, a1, max_tiles1, ns, st);
+}
+
 static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps &b2,
                        ExpertGemmArgs a1, ExpertGemmArgs a2, int max_tiles1, int max_tiles2,
                        cudaStream_t st, int stage1, int stage2, bool add)
@@ -412,9 +419,10 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
     const int ns = h->num_sms;
     {
         k3_stage sg(h, stage1, st);
-        rc = bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st)
-             : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true>(b1, a1, max_tiles1, ns, st)
-                         : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16>(b1, a1, max_tiles1, ns, st);
+        const int epi = a1.a8 ? EPI_A8 : a1.act.kind == K3MOE_ACT_SITU ? EPI_SITU : EPI_SILU;
+        rc = epi == EPI_A8     ? launch_glu<EPI_A8>(bn, b1, a1, max_tiles1, ns, st)
+             : epi == EPI_SITU ? launch_glu<EPI_SITU>(bn, b1, a1, max_tiles1, ns, st)
+                               : launch_glu<EPI_SILU>(bn, b1, a1, max_tiles1, ns, st);
         if (rc) return rc;
     }
     {

@@ -53,6 +53,9 @@ struct ExpertGemmArgs {
     int a8;                          // GLU: 1 rounds the output to MXFP8 (blocks of 32 rows per token)
 };
 
+// Epilogue variants of the GLU mode (a template argument of the kernel).
+enum { EPI_SILU = 0, EPI_SITU = 1, EPI_A8 = 2 };
+
 constexpr int EX_BM = 128;           // weight rows per tile (MMA M)
 constexpr int EX_KP = 256;           // K per packed stage (128-byte FP4 rows)
 constexpr int EX_KS = 64;            // K per MMA sub-step (one 128-byte f16 row)
@@ -120,7 +123,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int 
 constexpr int EX_NEPI = 8;
 __host__ __device__ constexpr int ex_threads(int nmat) { return (4 + 4 * nmat + EX_NEPI) * 32; }
 
-template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false>
+template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false, int EPI = 0>
 __global__ void __launch_bounds__(ex_threads(NMAT), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
@@ -454,8 +457,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             if (!role_wait(smem_u32(tfull + acc), (tc / NACC) & 1, abort_flag, lim, args.status, 7)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * NMAT * BN;
-            const bool situ = MODE == OUT_GLU_F16 && args.act.kind == K3MOE_ACT_SITU;
             const int nchunks = (nrows + 15) >> 4;
+            // the GLU variant (SiLU, SiTU, A8) is a template argument: each kernel carries one
+            constexpr int KIND = MODE == OUT_GLU_F16 ? EPI : EPI_SILU;
             for (int c = half; c < nchunks; c += NEPI / 4) {
                 // BF16_ADD: the chunk's addends are read before the TMEM loads, so
                 // their latency overlaps them
@@ -473,7 +477,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
                 tc_wait_ld();
-                if (MODE == OUT_GLU_F16 && args.a8) {
+                if constexpr (MODE == OUT_GLU_F16 && KIND == EPI_A8) {
                     // A8: the accurate activation, rounded to MXFP8 over the 32 consecutive
                     // weight rows this warp's lanes hold (one block of the down projection's K
                     // for each token): the 16 tokens' largest exponent fields, packed four to a
@@ -488,7 +492,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                             const float rs = srs[n];
                             const float gv = __uint_as_float(v0[j]) * (fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
-                            a = situ ? k3_glu(gv, uv, args.act) : __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            a = args.act.kind == K3MOE_ACT_SITU ? k3_glu(gv, uv, args.act)
+                                                                : __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                         }
                         av[j] = a;
                         pk[j >> 2] |= ((__float_as_uint(a) >> 23) & 0xFFu) << (8 * (j & 3));
@@ -507,37 +512,37 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                                 __float2half_rn(a);
                         }
                     }
-                    continue;
-                }
+                } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = c * 16 + j;
-                    if (n < nrows) {
-                        const size_t orow = (size_t)(row0 + n);
-                        if (MODE == OUT_GLU_F16) {
-                            // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
-                            // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
-                            // beta tanh(gv / beta) and soft-limits the up branch the same way
-                            const float rs = srs[n];
-                            const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
-                            const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
-                            float a;
-                            if (situ)
-                                a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
-                                    tanh_approx(hv * (2.0f * args.act.inv_beta)) *
-                                    (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
-                            else
-                                a = fmaf(hv, tanh_approx(hv), hv) * uv;
-                            bad |= !(fabsf(a) <= 65504.f);
-                            reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
-                        } else if (MODE == OUT_BF16) {
-                            uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                            o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
-                            if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * fw1);
-                        } else {
-                            uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                            o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * fw0);
-                            if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * fw1);
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = c * 16 + j;
+                        if (n < nrows) {
+                            const size_t orow = (size_t)(row0 + n);
+                            if (MODE == OUT_GLU_F16) {
+                                // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
+                                // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
+                                // beta tanh(gv / beta) and soft-limits the up branch the same way
+                                const float rs = srs[n];
+                                const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
+                                const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
+                                float a;
+                                if constexpr (KIND == EPI_SITU)
+                                    a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
+                                        tanh_approx(hv * (2.0f * args.act.inv_beta)) *
+                                        (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
+                                else
+                                    a = fmaf(hv, tanh_approx(hv), hv) * uv;
+                                bad |= !(fabsf(a) <= 65504.f);
+                                reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
+                            } else if (MODE == OUT_BF16) {
+                                uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
+                                o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
+                                if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * fw1);
+                            } else {
+                                uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
+                                o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * fw0);
+                                if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * fw1);
+                            }
                         }
                     }
                 }
