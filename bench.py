@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per touched expert per launch, from the ncu capture in
 # profiles/gemv_expert_decode_dram.md (decode GEMV, 128-expert case, scaled by
 # touched experts).  Valid only while those kernels are unchanged.
-NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.17e6, ("expert_down", "gemv"): 5.868e6}
+NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.08e6, ("expert_down", "gemv"): 5.866e6}
 
 
 def peaks():
