@@ -249,6 +249,164 @@ __global__ void __launch_bounds__(DN_THREADS, 2) dense_gemm_kernel(const __grid_
     }
 }
 
+// Decode sizes (T <= TNS tokens): weight-stationary form of the same product.
+// The MMA's M is 128 weight rows and its N the token count rounded to 16, so a
+// stage holds a 16 KB weight tile plus only TNS activation rows, and the ring
+// can be NS deep.  TMEM lanes are weight rows and columns tokens; the epilogue
+// writes fp32 partials [split][token][col0 + n] (split-K mode only).
+template <int TNS, int NS>
+struct DenseWsSmem {
+    static constexpr int A_BYTES = DN_BM * DN_BK * 2;   // 16 KB of weights
+    static constexpr int B_BYTES = TNS * DN_BK * 2;     // activation rows
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int OFF_BAR = NS * STAGE;
+    static constexpr int N_BAR = 2 * NS + 4 + 1;
+    static constexpr int BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;
+};
+
+template <int TNS, int NS>
+__global__ void __launch_bounds__(DN_THREADS, 2) dense_ws_kernel(const __grid_constant__ CUtensorMap amap,
+                                                               const __grid_constant__ CUtensorMap bmap0,
+                                                               const __grid_constant__ CUtensorMap bmap1,
+                                                               const DenseArgs args)
+{
+    griddep_enter();
+    using SM = DenseWsSmem<TNS, NS>;
+    constexpr uint32_t TMEM_COLS = 2 * TNS <= 32 ? 32 : 2 * TNS <= 64 ? 64 : 2 * TNS <= 128 ? 128 : 2 * TNS <= 256 ? 256 : 512;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + SM::OFF_BAR), *empty = full + NS;
+    uint64_t *tfull = empty + NS, *tempty = tfull + 2, *drain = tempty + 2;
+    uint32_t *tmem_holder = (uint32_t *)(drain + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tn = min(TNS, max(16, (args.M + 15) & ~15));      // MMA N
+    const int total = args.seg[0].n_tiles * args.seg[0].splits +
+                      (args.nseg > 1 ? args.seg[1].n_tiles * args.seg[1].splits : 0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(tfull + i), 1);
+            mbar_init(smem_u32(tempty + i), 8);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        prefetch_tmap(&amap);
+        prefetch_tmap(&bmap0);
+        if (args.nseg > 1) prefetch_tmap(&bmap1);
+        const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+            const DnTile d = dn_tile(args, t, 1, DN_BM);
+            const DenseSeg S = dn_seg(args, d.seg);
+            const CUtensorMap *bm = d.seg == 0 ? &bmap0 : &bmap1;
+            bool ok = true;
+            for (int s = 0; s < d.ks; ++s, ++it) {
+                const int slot = it % NS;
+                if (!dn_wait(smem_u32(empty + slot), ((it / NS) & 1) ^ 1, abort_flag, args.status, 25)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(full + slot);
+                mbar_expect_tx(fb, SM::STAGE);
+                uint8_t *st = smem + slot * SM::STAGE;
+                const int k = (d.k0 + s) * DN_BK;
+                tma_load_2d_hint(smem_u32(st), bm, fb, k, d.n0, pol_w);
+                tma_load_2d_hint(smem_u32(st + SM::A_BYTES), &amap, fb, k % S.a_kmod, 0, pol_a);
+            }
+            if (!ok) break;
+        }
+        const uint32_t n = it < (uint32_t)NS ? it : (uint32_t)NS;
+        for (uint32_t q = 0; q < n; ++q) {
+            const uint32_t i2 = it - 1 - q;
+            mbar_wait(smem_u32(full + i2 % NS), (i2 / NS) & 1, 0xFFFFFFFFu);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc = idesc_f16(DN_BM, tn, 1);
+        uint32_t it = 0, tc = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+            const DnTile d = dn_tile(args, t, 1, DN_BM);
+            const int acc = (int)(tc & 1);
+            if (!dn_wait(smem_u32(tempty + acc), ((tc >> 1) & 1) ^ 1, abort_flag, args.status, 26)) break;
+            tc_fence_after();
+            const uint32_t dcol = tmem + acc * TNS;
+            bool ok = true;
+            for (int s = 0; s < d.ks; ++s, ++it) {
+                const int slot = it % NS;
+                if (!dn_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, args.status, 27)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w_addr = smem_u32(smem + slot * SM::STAGE);
+                const uint64_t adesc = smem_desc_sw128(w_addr), bdesc = smem_desc_sw128(w_addr + SM::A_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < DN_BK / 16; ++kk)
+                    tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(smem_u32(empty + slot));
+            }
+            if (!ok) break;
+            tc_commit(smem_u32(tfull + acc));
+        }
+        tc_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, 0xFFFFFFFFu);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue (warps 2..9)
+        const int q = warp & 3;                       // TMEM lanes 32q .. 32q + 31 = weight rows
+        const int half = (warp - 2) >> 2;             // token chunks c with c % 2 == half
+        uint32_t tc = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+            const DnTile d = dn_tile(args, t, 1, DN_BM);
+            const DenseSeg S = dn_seg(args, d.seg);
+            const int acc = (int)(tc & 1);
+            const int n = d.n0 + 32 * q + lane;          // output column (weight row)
+            if (!dn_wait(smem_u32(tfull + acc), (tc >> 1) & 1, abort_flag, args.status, 28)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * TNS;
+            for (int c = half; c < tn / 16; c += 2) {
+                uint32_t v[16];
+                tmem_ld16(tbase + c * 16, v);
+                tc_wait_ld();
+                if (n < S.n_out) {
+                    float *o = reinterpret_cast<float *>(S.out) + ((size_t)d.split * args.M) * S.ldo + S.col0 + n;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = 16 * c + j;               // token
+                        if (m < args.M) o[(size_t)m * S.ldo] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // Sum split-K partials [splits][M][ldp] (columns [c0, c0 + n)) in split order.
 __global__ void dense_reduce_kernel(const float *__restrict__ part, int splits, int M, int ldp, int c0, int n,
                                    float *__restrict__ out32, uint16_t *__restrict__ out16, int ldo)
@@ -320,6 +478,40 @@ static int launch_dense(const CUtensorMap &a, const CUtensorMap &b0, const CUten
     k3_launch(kern, grid, DN_THREADS, SM::BYTES, st, a, b0, b1, args);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+template <int TNS, int NS>
+static int launch_dense_ws(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                           const DenseArgs &args, int num_sms, cudaStream_t st)
+{
+    using SM = DenseWsSmem<TNS, NS>;
+    static_assert(2 * (SM::BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
+    auto kern = dense_ws_kernel<TNS, NS>;
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
+    int tiles = 0;
+    for (int s = 0; s < args.nseg; ++s) tiles += args.seg[s].n_tiles * args.seg[s].splits;
+    if (tiles == 0) return K3MOE_OK;
+    const int grid = std::min(tiles, 2 * num_sms);
+    k3_launch(kern, grid, DN_THREADS, SM::BYTES, st, a, b0, b1, args);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+int k3_dense_ws_rows(int T) { return T <= 16 ? 16 : T <= 64 ? 64 : T <= 128 ? 128 : T <= 256 ? 256 : 0; }
+
+int k3_launch_dense_ws(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const DenseArgs &args,
+                       int num_sms, cudaStream_t st)
+{
+    for (int s = 0; s < args.nseg; ++s)
+        if (args.seg[s].mode != DN_OUT_F32 || args.seg[s].n_tiles * DN_BM < args.seg[s].n_out) return K3MOE_ERR_ARG;
+    switch (k3_dense_ws_rows(args.M)) {
+    case 16: return launch_dense_ws<16, 6>(a, b0, b1, args, num_sms, st);
+    case 64: return launch_dense_ws<64, 4>(a, b0, b1, args, num_sms, st);
+    case 128: return launch_dense_ws<128, 3>(a, b0, b1, args, num_sms, st);
+    case 256: return launch_dense_ws<256, 2>(a, b0, b1, args, num_sms, st);
+    default: return K3MOE_ERR_UNSUPPORTED;
+    }
 }
 
 int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,

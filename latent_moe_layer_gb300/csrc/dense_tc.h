@@ -32,6 +32,11 @@ struct DenseArgs {
 
 // X rows [rows, cols] BF16 (or weights): box 64 x box_rows, 128-byte swizzle.
 bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
+// Decode sizes (T <= 256): the weight-stationary kernel (MMA M = 128 weight rows, N =
+// tokens), split-K fp32 partials only.  a: x rows [T, K] with box rows k3_dense_ws_rows(T).
+int k3_dense_ws_rows(int T);
+int k3_launch_dense_ws(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const k3::DenseArgs &args,
+                       int num_sms, cudaStream_t st);
 int k3_launch_dense_tc(int bn, const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                        const k3::DenseArgs &args, int num_sms, cudaStream_t st);
 // out = sum over splits of part[s][m][c0 + j], j < n (fp32 and/or BF16 outputs, row stride ldo).

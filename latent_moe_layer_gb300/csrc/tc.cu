@@ -235,17 +235,18 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
     return K3MOE_OK;
 }
 
-// Split-K factors for one launch of the persistent dense GEMM (BN = 128 weight
-// rows per tile).  The kernel takes its units (segment 0's tiles first; per
-// tile its splits in order, the split sizes differing by at most one K step)
-// round-robin over `grid_max` CTAs.  Costs are in K steps (16 KB of weights):
-// a unit costs its K steps plus its fp32 partial tile (rows x 128 x 4 bytes =
-// rows / 32 K steps), and the reduction reads every partial once, spread over
-// the whole GPU.  The plan minimises the busiest CTA's load plus the
-// reduction; ties go to fewer units.
-static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max)
+// Split-K factors for one launch of a decode-size dense GEMM (128 weight rows per
+// tile): the weight-stationary kernel (ws: all T tokens in one MMA N) or the
+// token-major one (ceil(T / 128) token tiles).  The kernel takes its units
+// (segment 0's tiles first; per tile its splits in order, the split sizes
+// differing by at most one K step) round-robin over `grid_max` CTAs.  Costs are
+// in K steps (16 KB of weights): a unit costs its K steps plus its fp32 partial
+// tile (rows x 128 x 4 bytes = rows / 32 K steps), and the reduction reads every
+// partial once, spread over the whole GPU.  The plan minimises the busiest CTA's
+// load plus the reduction; ties go to fewer units.
+static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max, bool ws)
 {
-    const int mt = (T + 127) / 128;
+    const int mt = ws ? 1 : (T + 127) / 128;
     int ks_total[2], maxsp[2];
     for (int s = 0; s < nseg; ++s) {
         ks_total[s] = seg[s].K / 64;
@@ -269,7 +270,7 @@ static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max)
             for (int s = 0; s < nseg; ++s)
                 for (int t = 0; t < seg[s].n_tiles * mt * sp[s]; ++t, ++u) {
                     const int k = t % sp[s], m = (t / sp[s]) % mt;
-                    const int rows = std::min(128, T - 128 * m);
+                    const int rows = ws ? T : std::min(128, T - 128 * m);
                     load[u % grid] += (k + 1) * ks_total[s] / sp[s] - k * ks_total[s] / sp[s] + rows / 32.0;
                 }
             const double cost = *std::max_element(load.begin(), load.end()) + reduce / (16384.0 * grid_max);
@@ -284,15 +285,22 @@ static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max)
 }
 
 // Cached per token count in the handle (the plan depends only on T and the shapes).
-static void dense_splits(k3moe_handle *h, DenseSeg *seg, int nseg, int T, int slot)
+static void dense_splits(k3moe_handle *h, DenseSeg *seg, int nseg, int T, int slot, bool ws)
 {
     unsigned char *c = h->dense_splits[T] + slot;
     if (!c[0]) {
-        plan_splits(seg, nseg, T, 2 * h->num_sms);
+        plan_splits(seg, nseg, T, 2 * h->num_sms, ws);
         for (int s = 0; s < nseg; ++s) c[s] = (unsigned char)seg[s].splits;
     }
     for (int s = 0; s < nseg; ++s) seg[s].splits = c[s];
 }
+
+// Up to 64 tokens the decode-size dense GEMMs run weight-stationary: the token
+// tile of the token-major kernel would be mostly padding, and the smaller stage
+// allows a deeper ring (measured at T = 16: router + down_proj 22.7 -> 21.2 us,
+// up_proj 24.2 -> 19.4 us with stage events; at T = 256 the token-major kernel
+// is faster).
+static bool dense_ws(int T) { return T <= 64; }
 
 // Decode-size token counts use BN = 128 tiles and split-K into fp32 partials
 // (two CTAs per SM); larger counts use BN = 256 tiles writing outputs directly.
@@ -311,7 +319,9 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     const int bn = small ? 128 : 256;
     const bool hilo = c.router_dtype == K3MOE_ROUTER_F32;
     CUtensorMap ax, br, bd;
-    if (!k3_encode_bf16_rows(&ax, x, T, H, 128) ||
+    // decode sizes run the weight-stationary kernel, whose x tile holds only T rows (rounded up)
+    const bool ws_k = small && dense_ws(T);
+    if (!k3_encode_bf16_rows(&ax, x, T, H, ws_k ? k3_dense_ws_rows(T) : 128) ||
         !k3_encode_bf16_rows(&br, hilo ? (const void *)h->d_router_hilo : h->w_router, E, hilo ? 2 * H : H, bn) ||
         !k3_encode_bf16_rows(&bd, h->w_down, L, H, bn))
         return K3MOE_ERR_CUDA;
@@ -330,7 +340,7 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     d.a_kmod = H;
     if (small) {
         // split both segments so that the busiest CTA streams as few weight bytes as possible
-        dense_splits(h, a.seg, 2, T, 0);
+        dense_splits(h, a.seg, 2, T, 0, dense_ws(T));
         // partial columns: router [0, Ep), down [Ep, Ep + L); Ep rounds E to 16 floats
         r.mode = d.mode = DN_OUT_F32;
         r.out = d.out = ws.part;
@@ -351,7 +361,9 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
     int rc;
     {
         k3_stage sg(h, K3MOE_STAGE_ROUTER, st);
-        if ((rc = k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, h->num_sms, st))) return rc;
+        if ((rc = ws_k ? k3_launch_dense_ws(ax, br, bd, a, h->num_sms, st)
+                       : k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, h->num_sms, st)))
+            return rc;
     }
     if (small) {
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
@@ -370,7 +382,9 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     const bool small = dense_small(ws, T, (size_t)H);
     const int bn = small ? 128 : 256;
     CUtensorMap an, bu;
-    if (!k3_encode_bf16_rows(&an, ws.nrm, T, L, 128) || !k3_encode_bf16_rows(&bu, h->w_up, H, L, bn))
+    const bool ws_k = small && dense_ws(T);
+    if (!k3_encode_bf16_rows(&an, ws.nrm, T, L, ws_k ? k3_dense_ws_rows(T) : 128) ||
+        !k3_encode_bf16_rows(&bu, h->w_up, H, L, bn))
         return K3MOE_ERR_CUDA;
     DenseArgs a = {};
     a.nseg = 1;
@@ -385,9 +399,9 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.col0 = 0;
     u.ldo = H;
     u.splits = 1;
-    if (small) dense_splits(h, a.seg, 1, T, 2);
+    if (small) dense_splits(h, a.seg, 1, T, 2, dense_ws(T));
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
-    int rc = k3_launch_dense_tc(bn, an, bu, bu, a, h->num_sms, st);
+    int rc = ws_k ? k3_launch_dense_ws(an, bu, bu, a, h->num_sms, st) : k3_launch_dense_tc(bn, an, bu, bu, a, h->num_sms, st);
     if (rc) return rc;
     if (small)
         rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, out16 ? nullptr : ws.o32, out16, H, st);

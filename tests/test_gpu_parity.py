@@ -89,10 +89,11 @@ def test_wide_scale_exponents(path, T):
 
 
 # Token counts on each side of the tensor path's internal switches (SMALL_ALIGNED:
-# E = 24, K = 4): decode GEMV vs tcgen05 tiles at T K = 24 E (T = 144), split-K
-# dense GEMMs up to T = 256, the chunked permutation from T = 512, 192-row tiles
-# with the decoded weights in TMEM vs 256-row tiles at T K = 192 E (T = 1152).
-@pytest.mark.parametrize("T", [1, 144, 145, 256, 257, 511, 512, 1152, 1153, 2000])
+# E = 24, K = 4): the weight-stationary dense GEMMs up to T = 64, decode GEMV vs
+# tcgen05 tiles at T K = 24 E (T = 144), split-K dense GEMMs up to T = 256, the
+# chunked permutation from T = 512, 192-row tiles with the decoded weights in
+# TMEM vs 256-row tiles at T K = 192 E (T = 1152).
+@pytest.mark.parametrize("T", [1, 16, 17, 64, 65, 144, 145, 256, 257, 511, 512, 1152, 1153, 2000])
 def test_tensor_path_switch_boundaries(T):
     cfg = synth.SMALL_ALIGNED.with_tokens(T)
     g = run_gpu(cfg, TEN)
