@@ -79,7 +79,7 @@ struct ExpertSmem {
     static constexpr int OFF_PK = OFF_B + NB * B_BYTES;
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
     static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
-    static constexpr int OFF_RS = OFF_BAR + N_BAR * 8 + 16;          // after the tmem holder and abort flag
+    static constexpr int OFF_RS = (OFF_BAR + N_BAR * 8 + 16 + 15) & ~15;   // after the tmem holder and abort flag; 16-byte reads
     static constexpr int BYTES = OFF_RS + BN * 4 + 1024;              // + per-token factors + align slack
 };
 
@@ -473,6 +473,20 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         ad1[j] = ROWPAIR ? ar[row1] : 0.f;
                     }
                 }
+                // GLU: the chunk's 16 per-token factors, read from shared memory before
+                // any of the chunk's global stores (through generic pointers the compiler
+                // cannot order a shared read above an earlier store)
+                float rsv[16];
+                if constexpr (MODE == OUT_GLU_F16) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 f = reinterpret_cast<const float4 *>(srs + c * 16)[w];
+                        rsv[4 * w] = f.x;
+                        rsv[4 * w + 1] = f.y;
+                        rsv[4 * w + 2] = f.z;
+                        rsv[4 * w + 3] = f.w;
+                    }
+                }
                 uint32_t v0[16], v1[16];
                 tmem_ld16(tbase + c * 16, v0);
                 if (NMAT == 2) tmem_ld16(tbase + BN + c * 16, v1);
@@ -489,7 +503,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         const int n = c * 16 + j;
                         float a = 0.f;
                         if (n < nrows) {
-                            const float rs = srs[n];
+                            const float rs = rsv[j];
                             const float gv = __uint_as_float(v0[j]) * (fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                             a = args.act.kind == K3MOE_ACT_SITU ? k3_glu(gv, uv, args.act)
@@ -522,7 +536,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                                 // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
                                 // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
                                 // beta tanh(gv / beta) and soft-limits the up branch the same way
-                                const float rs = srs[n];
+                                const float rs = rsv[j];
                                 const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
                                 const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                                 float a;
