@@ -473,11 +473,12 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         ad1[j] = ROWPAIR ? ar[row1] : 0.f;
                     }
                 }
-                // GLU: the chunk's 16 per-token factors, read from shared memory before
-                // any of the chunk's global stores (through generic pointers the compiler
-                // cannot order a shared read above an earlier store)
+                // SiLU and SiTU: the chunk's 16 per-token factors, read from shared memory
+                // before any of the chunk's global stores (through generic pointers the
+                // compiler cannot order a shared read above an earlier store); A8 reads them
+                // in its first pass, which stores nothing
                 float rsv[16];
-                if constexpr (MODE == OUT_GLU_F16) {
+                if constexpr (MODE == OUT_GLU_F16 && KIND != EPI_A8) {
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 f = reinterpret_cast<const float4 *>(srs + c * 16)[w];
@@ -503,7 +504,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         const int n = c * 16 + j;
                         float a = 0.f;
                         if (n < nrows) {
-                            const float rs = rsv[j];
+                            const float rs = srs[n];
                             const float gv = __uint_as_float(v0[j]) * (fw0 * rs);
                             const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
                             a = args.act.kind == K3MOE_ACT_SITU ? k3_glu(gv, uv, args.act)
