@@ -258,6 +258,78 @@ size_t k3moe_qb_workspace_bytes(const k3moe_handle *h, int T, int nbins);
 int k3moe_qb_bias(k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
                   int nbins, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------ balanced expert-parallel plan
+ * The K3 report review, section "3T pre-training: turning irregular MoE into a
+ * static execution plan" (the MoonEP paragraph): with E experts on R
+ * expert-parallel ranks and at most E/R redundant expert slots per rank, a
+ * plan always exists in which every rank receives exactly S*K routed pairs
+ * (S tokens per rank, top-K routing), so the exchange buffers have a fixed
+ * size and no host read of token counts sits before the expert kernels.
+ * k3moe_ep_plan computes such a plan on the device from all ranks' per-expert
+ * counts; k3moe_ep_dispatch gives every routed pair of one source rank its
+ * destination rank and row.  The exchange itself (an all-to-all of S*K rows
+ * per rank, and the reverse one for the results) is the caller's.  They use
+ * the handle's n_experts, top_k and its device status word, which exists once
+ * k3moe_load_weights has run (K3MOE_ERR_STATE before).
+ *
+ * Rank r owns the m = E/R experts r*m .. r*m + m - 1.  The plan (the pages
+ * give the guarantee, not an algorithm): R times, the unplanned rank with the
+ * smallest remaining home load H (ties: lower rank) takes every remaining
+ * token of its home experts, then fills the rest of its C = S*K rows from the
+ * largest remaining experts (ties: lower expert index), whole experts first
+ * and a part of the last.  It never takes more than m experts for one rank:
+ * with n ranks left holding n*C tokens, the other ranks' m largest experts
+ * hold at least (n*C - H)/(n-1) >= C - H.  Expert e's pairs are numbered in
+ * (source rank, token) order and successive takes of e get successive ranges
+ * of that numbering, the home rank's share last.  A rank's C receive rows
+ * hold its segments in planning order (home experts in index order, then
+ * the takes), each a contiguous run.
+ *
+ * The plan, in caller-owned device buffers (int32):
+ *   seg      [2E][5]  segment i: expert, rank, src (first pair number of the
+ *                     expert it holds), count (> 0), dst (first receive row)
+ *   rank_seg [R][2]   rank r's segments are seg[first .. first + n)
+ *   exp_off  [E + 1]  expert e's segments are exp_seg[exp_off[e] .. exp_off[e + 1])
+ *   exp_seg  [2E]     segment ids grouped by expert, increasing src
+ *   info     [2]      number of segments; the most redundant experts on one rank
+ * A plan has at most 2E segments: one home segment and at most one take per
+ * expert and rank pair, at most E takes in all. */
+typedef struct {
+    int32_t *seg;
+    int32_t *rank_seg;
+    int32_t *exp_off;
+    int32_t *exp_seg;
+    int32_t *info;
+} k3moe_ep_plan;
+
+/* counts: device int32 [R][E], counts[q][e] = routed pairs of source rank q
+ * that select expert e (each rank's counts, all-gathered); their sum must be
+ * R * S * K and none negative.  tokens_per_rank: S.  n_ranks: R, 1 .. E with
+ * E % R == 0 and R * S * K below 2^31.  E up to 1024.
+ * One warp on the device; asynchronous on `stream`.  Errors: K3MOE_ERR_ARG
+ * (NULL pointers, bad sizes), K3MOE_ERR_UNSUPPORTED (E > 1024),
+ * K3MOE_ERR_STATE, K3MOE_ERR_CUDA.  Counts that are negative or do not sum to R * S * K are
+ * found on the device: the status word gets K3MOE_ERR_RANGE, info gets
+ * {0, -1} and the plan is not valid. */
+int k3moe_ep_plan_compute(k3moe_handle *h, const int32_t *counts, int n_ranks, int tokens_per_rank,
+                          const k3moe_ep_plan *plan, cudaStream_t stream);
+
+/* Destinations of source rank src_rank's routed pairs idx [S][K] (device int32,
+ * expert ids; the experts of one token distinct, as top-K gives): dest_rank
+ * and dest_row [S][K] (device int32), the rank whose expert copy processes the
+ * pair and its row in that rank's C receive rows.  counts and plan as given
+ * to k3moe_ep_plan_compute (counts[src_rank] must be this idx's per-expert
+ * counts).  workspace: caller-owned device memory of
+ * k3moe_ep_dispatch_workspace_bytes(h, S) bytes.  Asynchronous on `stream`.
+ * Errors: K3MOE_ERR_ARG, K3MOE_ERR_UNSUPPORTED (E > 1024 or K > 32),
+ * K3MOE_ERR_WORKSPACE, K3MOE_ERR_STATE, K3MOE_ERR_CUDA.  An expert id outside [0, E), counts
+ * that disagree with idx, or a pair number outside the plan set the status
+ * word to K3MOE_ERR_RANGE and that pair's outputs to -1. */
+size_t k3moe_ep_dispatch_workspace_bytes(const k3moe_handle *h, int tokens_per_rank);
+int k3moe_ep_dispatch(k3moe_handle *h, const int32_t *idx, int tokens_per_rank, int src_rank,
+                      const int32_t *counts, int n_ranks, const k3moe_ep_plan *plan, int32_t *dest_rank,
+                      int32_t *dest_row, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------ profiling
  * Stage timing with CUDA events recorded on the launching stream around each
  * stage of k3moe_forward (a ring of 256 forwards), plus a count of kernel

@@ -524,3 +524,51 @@ extern "C" int k3moe_qb_bias(k3moe_handle *h, const float *logits, int T, const 
     if (dev != h->device) return K3MOE_ERR_STATE;
     return k3_qb_bias(h, logits, T, bias_in, bias_out, nbins, workspace, workspace_bytes, stream);
 }
+
+static int ep_check(const k3moe_handle *h, int n_ranks, int S)
+{
+    if (!h) return K3MOE_ERR_ARG;
+    if (!h->loaded) return K3MOE_ERR_STATE;
+    const int E = h->cfg.n_experts, K = h->cfg.top_k;
+    if (E > 1024 || K > 32) return K3MOE_ERR_UNSUPPORTED;
+    if (n_ranks < 1 || n_ranks > E || E % n_ranks || S < 1) return K3MOE_ERR_ARG;
+    if ((long long)n_ranks * S * K >= (1LL << 31)) return K3MOE_ERR_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return K3MOE_ERR_CUDA;
+    if (dev != h->device) return K3MOE_ERR_STATE;
+    return K3MOE_OK;
+}
+
+static bool ep_plan_ok(const k3moe_ep_plan *p)
+{
+    return p && p->seg && p->rank_seg && p->exp_off && p->exp_seg && p->info;
+}
+
+extern "C" int k3moe_ep_plan_compute(k3moe_handle *h, const int32_t *counts, int n_ranks, int tokens_per_rank,
+                                     const k3moe_ep_plan *plan, cudaStream_t stream)
+{
+    if (!counts || !ep_plan_ok(plan)) return K3MOE_ERR_ARG;
+    const int rc = ep_check(h, n_ranks, tokens_per_rank);
+    if (rc) return rc;
+    return k3_ep_plan(h, counts, n_ranks, tokens_per_rank * h->cfg.top_k, plan, stream);
+}
+
+extern "C" size_t k3moe_ep_dispatch_workspace_bytes(const k3moe_handle *h, int tokens_per_rank)
+{
+    if (!h || tokens_per_rank < 1 || (long long)tokens_per_rank * h->cfg.top_k >= (1LL << 31)) return 0;
+    return k3_ep_dispatch_workspace_bytes(tokens_per_rank, h->cfg.n_experts);
+}
+
+extern "C" int k3moe_ep_dispatch(k3moe_handle *h, const int32_t *idx, int tokens_per_rank, int src_rank,
+                                 const int32_t *counts, int n_ranks, const k3moe_ep_plan *plan, int32_t *dest_rank,
+                                 int32_t *dest_row, void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!idx || !counts || !dest_rank || !dest_row || !ep_plan_ok(plan)) return K3MOE_ERR_ARG;
+    const int rc = ep_check(h, n_ranks, tokens_per_rank);
+    if (rc) return rc;
+    if (src_rank < 0 || src_rank >= n_ranks) return K3MOE_ERR_ARG;
+    if (!workspace || workspace_bytes < k3_ep_dispatch_workspace_bytes(tokens_per_rank, h->cfg.n_experts))
+        return K3MOE_ERR_WORKSPACE;
+    return k3_ep_dispatch(h, idx, tokens_per_rank, src_rank, counts, n_ranks, plan, dest_rank, dest_row, workspace,
+                          stream);
+}

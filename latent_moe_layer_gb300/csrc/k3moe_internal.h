@@ -276,6 +276,14 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws);  // base 
 // routing and permutation (route.cu)
 int k3_launch_topk(const k3moe_handle *h, const float *logits, int T, int32_t *idx, float *wts,
                    int32_t *counts_zero, cudaStream_t st);   // counts_zero: [E] set to 0, or NULL
+void k3_launch_chunk_count(const int32_t *idx, int T, int K, int E, int32_t *chunk_cnt, int32_t *totals,
+                           int *status, cudaStream_t st);
+void k3_launch_chunk_base(int T, int E, const int32_t *base, int32_t *chunk_cnt, cudaStream_t st);
+size_t k3_ep_dispatch_workspace_bytes(int T, int E);
+int k3_ep_plan(const k3moe_handle *h, const int32_t *counts, int R, int C, const k3moe_ep_plan *plan,
+               cudaStream_t st);
+int k3_ep_dispatch(const k3moe_handle *h, const int32_t *idx, int T, int src, const int32_t *counts, int R,
+                   const k3moe_ep_plan *plan, int32_t *dest_rank, int32_t *dest_row, void *ws, cudaStream_t st);
 size_t k3_qb_workspace_bytes(int T, int E, int nbins);
 int k3_qb_bias(const k3moe_handle *h, const float *logits, int T, const float *bias_in, float *bias_out,
                int nbins, void *ws, size_t ws_bytes, cudaStream_t st);

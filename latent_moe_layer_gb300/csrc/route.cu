@@ -426,6 +426,25 @@ int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStr
     return k3_launch_permute(h, ws, T, tile_n, st);
 }
 
+// The chunked stable numbering of a routing's pairs on its own: per-chunk
+// expert counts (and totals added into `totals`), then each chunk's first
+// number of each expert counted from base[e].  Used by the expert-parallel
+// dispatch, whose numbers continue those of the lower source ranks.
+void k3_launch_chunk_count(const int32_t *idx, int T, int K, int E, int32_t *chunk_cnt, int32_t *totals,
+                           int *status, cudaStream_t st)
+{
+    const int nch = (T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK;
+    k3_launch(perm_chunk_count_kernel, nch, 256, sizeof(int) * E, st, idx, T, K, E, nch, chunk_cnt, totals, status);
+    k3_note_launch();
+}
+
+void k3_launch_chunk_base(int T, int E, const int32_t *base, int32_t *chunk_cnt, cudaStream_t st)
+{
+    const int nch = (T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK;
+    k3_launch(perm_chunk_base_kernel, E, 1024, 0, st, nch, base, chunk_cnt);
+    k3_note_launch();
+}
+
 int k3_launch_permute(const k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStream_t st)
 {
     const int E = h->cfg.n_experts, K = h->cfg.top_k, n = T * K;

@@ -26,7 +26,7 @@ EXPORTS = ["k3moe_create", "k3moe_persistent_bytes", "k3moe_load_weights", "k3mo
            "k3moe_forward", "k3moe_forward_host", "k3moe_status", "k3moe_destroy", "k3moe_strerror",
            "k3moe_path_for", "k3moe_debug_dequant", "k3moe_debug_wait_timeout",
            "k3moe_profile_enable", "k3moe_profile_read", "k3moe_stage_name", "k3moe_qb_workspace_bytes",
-           "k3moe_qb_bias"]
+           "k3moe_qb_bias", "k3moe_ep_plan_compute", "k3moe_ep_dispatch_workspace_bytes", "k3moe_ep_dispatch"]
 STAGES = ["router", "down_proj", "topk", "permute", "gate_up", "expert_down", "combine_norm",
           "up_proj", "shared", "finish", "prep", "shared_down"]
 
@@ -58,6 +58,12 @@ class Weights(C.Structure):
 
 
 _lib = None
+
+
+class EpPlan(C.Structure):
+    """k3moe_ep_plan: device pointers of a balanced expert-parallel plan."""
+    _fields_ = [("seg", C.c_void_p), ("rank_seg", C.c_void_p), ("exp_off", C.c_void_p),
+                ("exp_seg", C.c_void_p), ("info", C.c_void_p)]
 
 
 def lib():
@@ -92,6 +98,10 @@ def lib():
         L.k3moe_qb_workspace_bytes.argtypes = [vp, i, i]
         L.k3moe_qb_workspace_bytes.restype = sz
         L.k3moe_qb_bias.argtypes = [vp, vp, i, vp, vp, i, vp, sz, vp]
+        L.k3moe_ep_plan_compute.argtypes = [vp, vp, i, i, C.POINTER(EpPlan), vp]
+        L.k3moe_ep_dispatch_workspace_bytes.argtypes = [vp, i]
+        L.k3moe_ep_dispatch_workspace_bytes.restype = sz
+        L.k3moe_ep_dispatch.argtypes = [vp, vp, i, i, vp, i, C.POINTER(EpPlan), vp, vp, vp, sz, vp]
         for name in EXPORTS:
             getattr(L, name)
         _lib = L
@@ -227,8 +237,45 @@ class Layer:
                                   ws.data_ptr(), n, _stream_ptr(stream)), "qb_bias")
         return out
 
+    def ep_plan(self, counts, tokens_per_rank, stream=None):
+        """Balanced expert-parallel plan from all ranks' per-expert counts (int32
+        CUDA [R, E]) -> dict of int32 CUDA tensors seg [2E, 5] (expert, rank,
+        src, count, dst), rank_seg [R, 2], exp_off [E + 1], exp_seg [2E], info [2]."""
+        import torch
+        R, E = counts.shape
+        dev = counts.device
+        plan = dict(seg=torch.empty((2 * E, 5), dtype=torch.int32, device=dev),
+                    rank_seg=torch.empty((R, 2), dtype=torch.int32, device=dev),
+                    exp_off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    exp_seg=torch.empty(2 * E, dtype=torch.int32, device=dev),
+                    info=torch.empty(2, dtype=torch.int32, device=dev))
+        check(lib().k3moe_ep_plan_compute(self.h, counts.data_ptr(), R, tokens_per_rank,
+                                          C.byref(_ep_struct(plan)), _stream_ptr(stream)), "ep_plan")
+        return plan
+
+    def ep_dispatch(self, idx, src_rank, counts, plan, stream=None):
+        """Destinations (rank, row) of source rank src_rank's routed pairs idx
+        (int32 CUDA [S, K]) under `plan` -> two int32 CUDA tensors [S, K]."""
+        import torch
+        S = idx.shape[0]
+        n = lib().k3moe_ep_dispatch_workspace_bytes(self.h, S)
+        if n == 0:
+            raise K3Error(ERR_CODE["ARG"], "ep_dispatch_workspace_bytes")
+        ws = torch.empty(n, dtype=torch.uint8, device=idx.device)
+        rank = torch.empty_like(idx)
+        row = torch.empty_like(idx)
+        check(lib().k3moe_ep_dispatch(self.h, idx.data_ptr(), S, src_rank, counts.data_ptr(), counts.shape[0],
+                                      C.byref(_ep_struct(plan)), rank.data_ptr(), row.data_ptr(), ws.data_ptr(), n,
+                                      _stream_ptr(stream)), "ep_dispatch")
+        return rank, row
+
     def debug_wait_timeout(self, spin_limit, stream=None):
         check(lib().k3moe_debug_wait_timeout(self.h, spin_limit, _stream_ptr(stream)), "wait")
+
+
+def _ep_struct(plan):
+    return EpPlan(plan["seg"].data_ptr(), plan["rank_seg"].data_ptr(), plan["exp_off"].data_ptr(),
+                  plan["exp_seg"].data_ptr(), plan["info"].data_ptr())
 
 
 def debug_dequant(packed, scale, stream=None):

@@ -106,3 +106,22 @@ def test_debug_dequant_argument_checks(lib):
     assert lib.k3moe_debug_dequant(None, None, 1, 32, None, None) == -1
     one = C.c_void_p(16)
     assert lib.k3moe_debug_dequant(one, one, 1, 33, one, None) == -2
+
+
+def test_ep_plan_argument_checks(lib):
+    from latent_moe_layer_gb300 import k3moe
+    rc, h = _create(lib, _cfg())
+    try:
+        one = C.c_void_p(16)
+        plan = k3moe.EpPlan(16, 16, 16, 16, 16)
+        empty = k3moe.EpPlan(16, 16, 16, None, 16)
+        assert lib.k3moe_ep_plan_compute(h, None, 8, 16, C.byref(plan), None) == -1
+        assert lib.k3moe_ep_plan_compute(h, one, 8, 16, C.byref(empty), None) == -1
+        assert lib.k3moe_ep_plan_compute(h, one, 8, 16, C.byref(plan), None) == -11   # no weights: no status word
+        assert lib.k3moe_ep_dispatch(h, one, 16, 0, one, 8, C.byref(plan), one, one, one, 1 << 20, None) == -11
+        assert lib.k3moe_ep_dispatch(h, None, 16, 0, one, 8, C.byref(plan), one, one, one, 1 << 20, None) == -1
+        # 896 experts, 16 tokens: 1 chunk of per-expert counts plus the bases and totals
+        assert lib.k3moe_ep_dispatch_workspace_bytes(h, 16) >= 3 * 896 * 4
+        assert lib.k3moe_ep_dispatch_workspace_bytes(h, 0) == 0
+    finally:
+        lib.k3moe_destroy(h)
