@@ -375,6 +375,54 @@ def run_ours(args):
                    "achieved_gbs": round(qbytes / (qms / 1e3) / 1e9, 1),
                    "frac": round(qbytes / (qms / 1e3) / 1e9 / pk["hbm_gbs"], 4), "nbins": 1000}
 
+    # Balanced expert-parallel plan and dispatch (the MoonEP step around the
+    # experts), prefill batches only: R ranks each routing this workload's T
+    # tokens (top-K of seeded N(0, 1) logits); one source rank's dispatch timed
+    ep_line = None
+    if cfg.T >= 4096 and not args.no_ep:
+        ep_line = {}
+        g = torch.Generator(device="cuda").manual_seed(9)
+        for R in (8, 64):
+            if cfg.E % R:
+                continue
+            cnt = torch.empty((R, cfg.E), dtype=torch.int32, device="cuda")
+            idx0 = None
+            for q in range(R):
+                lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda")
+                top = torch.topk(lg, cfg.K, dim=1).indices.to(torch.int32).contiguous()
+                cnt[q] = torch.bincount(top.flatten(), minlength=cfg.E).to(torch.int32)
+                if q == 0:
+                    idx0 = top
+            for _ in range(3):
+                plan = layer.ep_plan(cnt, cfg.T)
+                layer.ep_dispatch(idx0, 0, cnt, plan)
+            n_rep = 20
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+            torch.cuda.synchronize()
+            for q0, q1 in ev:
+                q0.record()
+                plan = layer.ep_plan(cnt, cfg.T)
+                q1.record()
+            torch.cuda.synchronize()
+            plan_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
+            for q0, q1 in ev:
+                flush.zero_()
+                q0.record()
+                layer.ep_dispatch(idx0, 0, cnt, plan)
+                q1.record()
+            torch.cuda.synchronize()
+            disp_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
+            if layer.status() != 0:
+                raise RuntimeError("expert-parallel plan or dispatch reported a device error")
+            info = plan["info"].tolist()
+            pairs = cfg.T * cfg.K
+            dbytes = 12 * pairs                         # idx read, destination rank and row written
+            ep_line[f"ranks_{R}"] = {
+                "tokens_per_rank": cfg.T, "plan_us": round(plan_ms * 1e3, 1), "dispatch_us": round(disp_ms * 1e3, 1),
+                "segments": info[0], "max_redundant_experts": info[1], "redundant_slots_per_rank": cfg.E // R,
+                "dispatch_algorithmic_bytes": dbytes,
+                "dispatch_gbs": round(dbytes / (disp_ms / 1e3) / 1e9, 1), "dispatch_launches": 4}
+
     exp_ms = stage_ms["gate_up"] + stage_ms["expert_down"]
     detail = {
         "stage_ms_per_step": {k: round(v / max(1, nfw), 4) for k, v in stage_ms.items() if v > 0},
@@ -387,6 +435,8 @@ def run_ours(args):
     }
     if qb_line:
         detail["qb_bias_update"] = qb_line
+    if ep_line:
+        detail["expert_parallel_plan"] = ep_line
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -507,6 +557,7 @@ def main():
     ap.add_argument("--a8", action="store_true", help="MXFP8 activations into the routed experts (the A8 option)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ep", action="store_true", help="skip the expert-parallel plan timing (prefill configs)")
     ap.add_argument("--library-peaks", action="store_true",
                     help="print the vendor library's dense BF16 / FP8 / MXFP8 GEMM rates and exit")
     args = ap.parse_args()
