@@ -3,19 +3,21 @@
 // MoonEP paragraph): with E experts on R ranks and at most E/R redundant
 // expert slots per rank, every rank can receive exactly C = S*K routed pairs.
 //
-// Plan: one warp, all state in shared memory.  R rounds; each takes the
-// unplanned rank with the smallest remaining home load H (warp minimum over
-// the ranks), gives it its home experts' remaining pairs (ballot + scan for
-// the segment slots and receive rows), then fills its C - H remaining rows
-// from the largest remaining experts, one warp maximum per take.  At most
-// E/R takes per rank (the other ranks' E/R largest experts hold at least
-// C - H), at most E takes in all, at most 2E segments.
+// Plan: one CTA; all state in shared memory.  The CTA sums the count matrix;
+// then one warp runs R rounds.  Each takes the unplanned rank with the
+// smallest remaining home load H (warp minimum over the ranks), gives it its
+// home experts' remaining pairs (ballot + scan for the segment slots and
+// receive rows), then fills its C - H remaining rows from the largest
+// remaining experts, one warp maximum over the lanes' block maxima per take.
+// At most E/R takes per rank (the other ranks' E/R largest experts hold at
+// least C - H), at most E takes in all, at most 2E segments.
 //
 // Dispatch of one source rank's pairs: expert e's pairs are numbered in
 // (source rank, token) order, so this rank's continue from the counts of the
 // lower ranks.  The routing's chunked stable numbering (the same kernels as
 // the permutation) gives each pair its number j; a binary search over the
-// expert's segments (increasing src) finds the one holding j.
+// expert's segments (increasing src, staged in shared memory) finds the one
+// holding j.
 #include "k3moe_internal.h"
 
 namespace k3 {
@@ -53,50 +55,77 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane)
 }
 
 // Shared memory: rem, taken, nseg_of [E]; seg_expert, seg_ord [2E]; H [R].
-__global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__ counts, int R, int E, int C,
-                                                     int32_t *__restrict__ seg, int32_t *__restrict__ rank_seg,
-                                                     int32_t *__restrict__ exp_off, int32_t *__restrict__ exp_seg,
-                                                     int32_t *__restrict__ info, int *status)
+// All EP_PLAN_THREADS threads sum the counts (a thread per expert, reads
+// coalesced over the experts) and the home loads; warp 0 then runs the rounds.
+// Lane l owns experts [l*B, l*B + B) and keeps the largest (count, -index) key
+// of its block, refreshed only when a count in the block changes.
+constexpr int EP_PLAN_THREADS = 1024;
+
+__global__ void __launch_bounds__(EP_PLAN_THREADS) ep_plan_kernel(const int32_t *__restrict__ counts, int R, int E,
+                                                                  int C, int32_t *__restrict__ seg,
+                                                                  int32_t *__restrict__ rank_seg,
+                                                                  int32_t *__restrict__ exp_off,
+                                                                  int32_t *__restrict__ exp_seg,
+                                                                  int32_t *__restrict__ info, int *status)
 {
     griddep_enter();
     extern __shared__ int ep_sm[];
+    __shared__ long long part[EP_PLAN_THREADS / 32];
     int *rem = ep_sm, *taken = rem + E, *nseg_of = taken + E;
     int *seg_expert = nseg_of + E, *seg_ord = seg_expert + 2 * E, *H = seg_ord + 2 * E;
-    const int lane = threadIdx.x, m = E / R;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, m = E / R;
+    const long long cap = (long long)R * C;
 
     // per-expert totals over the source ranks
-    long long tot = 0;
+    long long s = 0;
     bool bad = false;
-    for (int e = lane; e < E; e += 32) {
-        long long s = 0;
+    if (tid < E) {
+#pragma unroll 8
         for (int q = 0; q < R; ++q) {
-            const int v = counts[(size_t)q * E + e];
+            const int v = counts[(size_t)q * E + tid];
             bad |= v < 0;
             s += v;
         }
-        bad |= s > (long long)R * C;
-        rem[e] = (int)(s > (long long)R * C ? 0 : s);
-        taken[e] = 0;
-        nseg_of[e] = 0;
-        tot += s;
+        bad |= s > cap;
+        rem[tid] = (int)(s > cap ? 0 : s);
+        taken[tid] = 0;
+        nseg_of[tid] = 0;
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if (__any_sync(0xffffffffu, bad) || tot != (long long)R * C) {
-        if (lane == 0) {
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) part[warp] = s;
+    bad = __syncthreads_or(bad);
+    long long tot = 0;
+    for (int w = 0; w < EP_PLAN_THREADS / 32; ++w) tot += part[w];
+    if (bad || tot != cap) {
+        if (tid == 0) {
             set_status(status, K3MOE_ERR_RANGE, -1);
             info[0] = 0;
             info[1] = -1;
         }
         return;
     }
-    __syncwarp();
-    for (int r = lane; r < R; r += 32) {
+    if (tid < R) {
         int h = 0;
-        for (int i = 0; i < m; ++i) h += rem[r * m + i];
-        H[r] = h;                                     // -1 once planned
+        for (int i = 0; i < m; ++i) h += rem[tid * m + i];
+        H[tid] = h;                                   // -1 once planned
     }
-    __syncwarp();
+    __syncthreads();
+    if (warp != 0) return;
+
+    const int B = (E + 31) / 32, blo = min(E, lane * B), bhi = min(E, blo + B);
+    auto block_top = [&]() {
+        unsigned long long k = 0;
+        for (int e = blo; e < bhi; ++e) {
+            const int v = rem[e];
+            if (v > 0) {
+                const unsigned long long kk = ((unsigned long long)(unsigned)v << 32) | (unsigned)(E - 1 - e);
+                k = kk > k ? kk : k;
+            }
+        }
+        return k;
+    };
+    unsigned long long mine = block_top();
 
     int nseg = 0, max_red = 0;
     for (int round = 0; round < R; ++round) {
@@ -118,15 +147,15 @@ __global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__
             const unsigned has = __ballot_sync(0xffffffffu, v > 0);
             const int incl = warp_incl_scan(v, lane);
             if (v > 0) {
-                const int s = nseg + __popc(has & ((1u << lane) - 1u));
-                int32_t *o = seg + (size_t)s * EP_SEG_INTS;
+                const int sl = nseg + __popc(has & ((1u << lane) - 1u));
+                int32_t *o = seg + (size_t)sl * EP_SEG_INTS;
                 o[0] = e;
                 o[1] = r;
                 o[2] = taken[e];
                 o[3] = v;
                 o[4] = dst + incl - v;
-                seg_expert[s] = e;
-                seg_ord[s] = nseg_of[e]++;
+                seg_expert[sl] = e;
+                seg_ord[sl] = nseg_of[e]++;
                 taken[e] += v;
                 rem[e] = 0;
             }
@@ -134,19 +163,12 @@ __global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__
             dst += __shfl_sync(0xffffffffu, incl, 31);
         }
         __syncwarp();
+        if (blo < (r + 1) * m && bhi > r * m) mine = block_top();
         if (lane == 0) H[r] = -1;
         int takes = 0;
         while (need > 0) {
             // the largest remaining expert; equal counts: the lower index
-            unsigned long long top = 0;
-            for (int e = lane; e < E; e += 32) {
-                const int v = rem[e];
-                if (v > 0) {
-                    const unsigned long long k = ((unsigned long long)(unsigned)v << 32) | (unsigned)(E - 1 - e);
-                    top = k > top ? k : top;
-                }
-            }
-            top = warp_max_u64(top);
+            const unsigned long long top = warp_max_u64(mine);
             if (top == 0 || takes == m) {             // excluded by the bound; kept as a guard
                 if (lane == 0) {
                     set_status(status, K3MOE_ERR_RANGE, -2);
@@ -156,7 +178,7 @@ __global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__
                 return;
             }
             const int e = E - 1 - (int)(top & 0xffffffffu), v = (int)(top >> 32), t = min(v, need);
-            if (lane == 0) {
+            if (e >= blo && e < bhi) {               // the owner lane updates the expert
                 int32_t *o = seg + (size_t)nseg * EP_SEG_INTS;
                 o[0] = e;
                 o[1] = r;
@@ -168,6 +190,7 @@ __global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__
                 taken[e] += t;
                 rem[e] = v - t;
                 H[e / m] -= t;
+                mine = block_top();
             }
             __syncwarp();
             ++nseg;
@@ -196,7 +219,7 @@ __global__ void __launch_bounds__(32) ep_plan_kernel(const int32_t *__restrict__
         carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     __syncwarp();
-    for (int s = lane; s < nseg; s += 32) exp_seg[nseg_of[seg_expert[s]] + seg_ord[s]] = s;
+    for (int i = lane; i < nseg; i += 32) exp_seg[nseg_of[seg_expert[i]] + seg_ord[i]] = i;
     if (lane == 0) {
         exp_off[E] = carry;
         info[0] = nseg;
@@ -218,26 +241,60 @@ __global__ void ep_base_kernel(const int32_t *__restrict__ counts, int E, int sr
     totals[e] = 0;
 }
 
-// One warp per chunk of tokens, in token order; lane k numbers pair (t, k).
+// EP_DISPATCH_WARPS chunks of 32 tokens per CTA, one warp each, in token
+// order; lane k numbers pair (t, k).  The plan's segments, in expert order,
+// are staged in shared memory (src, rank, dst) beside each expert's first
+// slot; every index read from the plan is checked before use, so a plan that
+// failed on the device yields -1 destinations and a status, not stray reads.
 // Block 0 also checks the routing's totals against counts[src].
-__global__ void __launch_bounds__(32) ep_dispatch_kernel(const int32_t *__restrict__ idx, int T, int K, int E,
-                                                         int nch, const int32_t *__restrict__ chunk_base,
-                                                         const int32_t *__restrict__ totals,
-                                                         const int32_t *__restrict__ own_counts,
-                                                         const int32_t *__restrict__ seg,
-                                                         const int32_t *__restrict__ exp_off,
-                                                         const int32_t *__restrict__ exp_seg,
-                                                         int32_t *__restrict__ dest_rank,
-                                                         int32_t *__restrict__ dest_row, int *status)
+constexpr int EP_DISPATCH_WARPS = 4;
+
+__global__ void __launch_bounds__(32 * EP_DISPATCH_WARPS)
+    ep_dispatch_kernel(const int32_t *__restrict__ idx, int T, int K, int E, int R, int nch,
+                       const int32_t *__restrict__ chunk_base, const int32_t *__restrict__ totals,
+                       const int32_t *__restrict__ own_counts, const int32_t *__restrict__ seg,
+                       const int32_t *__restrict__ exp_off, const int32_t *__restrict__ exp_seg,
+                       const int32_t *__restrict__ info, int32_t *__restrict__ dest_rank,
+                       int32_t *__restrict__ dest_row, int *status)
 {
     griddep_enter();
-    extern __shared__ int next[];                    // [E] next pair number per expert
-    const int ch = blockIdx.x, lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32) {
-        next[e] = chunk_base[(size_t)e * nch + ch];
-        if (ch == 0 && totals[e] != own_counts[e]) set_status(status, K3MOE_ERR_RANGE, -3);
+    extern __shared__ int ep_dsm[];
+    int *toff = ep_dsm;                              // [E + 1]
+    int *tsrc = toff + E + 1, *tend = tsrc + 2 * E, *trank = tend + 2 * E, *tdst = trank + 2 * E;   // [2E] each
+    int *next = tdst + 2 * E;                        // [EP_DISPATCH_WARPS][E]
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int C = T * K;
+    int n = info[0];
+    const bool plan_ok = n >= 1 && n <= 2 * E;
+    n = plan_ok ? n : 0;
+    for (int e = tid; e <= E; e += blockDim.x) {
+        int o = plan_ok ? exp_off[e] : 0;
+        toff[e] = (o < 0 || o > n) ? 0 : o;
     }
-    __syncwarp();
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int sid = exp_seg[i];
+        int src = 0, end = 0, rk = -1, dst = 0;
+        if (sid >= 0 && sid < n) {
+            const int32_t *g = seg + (size_t)sid * EP_SEG_INTS;
+            src = g[2];
+            end = g[2] + g[3];
+            rk = g[1];
+            dst = g[4];
+            if (rk < 0 || rk >= R || g[3] <= 0 || dst < 0 || dst > C - g[3]) rk = -1;
+        }
+        tsrc[i] = src;
+        tend[i] = end;
+        trank[i] = rk;
+        tdst[i] = dst;
+    }
+    const int ch = blockIdx.x * EP_DISPATCH_WARPS + w;
+    int *nx = next + w * E;
+    for (int e = lane; e < E; e += 32) {
+        if (ch < nch) nx[e] = chunk_base[(size_t)e * nch + ch];
+        if (blockIdx.x == 0 && w == 0 && totals[e] != own_counts[e]) set_status(status, K3MOE_ERR_RANGE, -3);
+    }
+    __syncthreads();
+    if (ch >= nch) return;
     const int t1 = min(T, (ch + 1) * K3_PERM_CHUNK);
     for (int t = ch * K3_PERM_CHUNK; t < t1; ++t) {
         if (lane < K) {
@@ -245,18 +302,17 @@ __global__ void __launch_bounds__(32) ep_dispatch_kernel(const int32_t *__restri
             const int e = idx[p];
             int rk = -1, row = -1;
             if (e >= 0 && e < E) {
-                const int j = atomicAdd(&next[e], 1);  // distinct experts per token: token order
-                int lo = exp_off[e], hi = exp_off[e + 1];
+                const int j = atomicAdd(&nx[e], 1);     // distinct experts per token: token order
+                int lo = toff[e], hi = toff[e + 1];
                 if (lo < hi) {
-                    while (hi - lo > 1) {              // last segment with src <= j
+                    while (hi - lo > 1) {               // last segment with src <= j
                         const int mid = (lo + hi) >> 1;
-                        if (seg[(size_t)exp_seg[mid] * EP_SEG_INTS + 2] <= j) lo = mid;
+                        if (tsrc[mid] <= j) lo = mid;
                         else hi = mid;
                     }
-                    const int32_t *g = seg + (size_t)exp_seg[lo] * EP_SEG_INTS;
-                    if (j >= g[2] && j < g[2] + g[3]) {
-                        rk = g[1];
-                        row = g[4] + (j - g[2]);
+                    if (j >= tsrc[lo] && j < tend[lo] && trank[lo] >= 0) {
+                        rk = trank[lo];
+                        row = tdst[lo] + (j - tsrc[lo]);
                     }
                 }
             }
@@ -279,8 +335,8 @@ int k3_ep_plan(const k3moe_handle *h, const int32_t *counts, int R, int C, const
 {
     const int E = h->cfg.n_experts;
     const size_t smem = sizeof(int) * (size_t)(7 * E + R);
-    k3_launch(ep_plan_kernel, 1, 32, smem, st, counts, R, E, C, plan->seg, plan->rank_seg, plan->exp_off,
-              plan->exp_seg, plan->info, h->d_status);
+    k3_launch(ep_plan_kernel, 1, EP_PLAN_THREADS, smem, st, counts, R, E, C, plan->seg, plan->rank_seg,
+              plan->exp_off, plan->exp_seg, plan->info, h->d_status);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
@@ -294,7 +350,6 @@ size_t k3_ep_dispatch_workspace_bytes(int T, int E)
 int k3_ep_dispatch(const k3moe_handle *h, const int32_t *idx, int T, int src, const int32_t *counts, int R,
                    const k3moe_ep_plan *plan, int32_t *dest_rank, int32_t *dest_row, void *ws, cudaStream_t st)
 {
-    (void)R;
     const int E = h->cfg.n_experts, K = h->cfg.top_k;
     const int nch = (T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK;
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -307,8 +362,15 @@ int k3_ep_dispatch(const k3moe_handle *h, const int32_t *idx, int T, int src, co
     k3_note_launch();
     k3_launch_chunk_count(idx, T, K, E, chunk_cnt, totals, h->d_status, st);
     k3_launch_chunk_base(T, E, base, chunk_cnt, st);
-    k3_launch(ep_dispatch_kernel, nch, 32, sizeof(int) * E, st, idx, T, K, E, nch, chunk_cnt, totals,
-              counts + (size_t)src * E, plan->seg, plan->exp_off, plan->exp_seg, dest_rank, dest_row, h->d_status);
+    // the segment table (E + 1 offsets, 4 x 2E fields) and a counter row per warp: 53 KB at E = 1024
+    const size_t smem = sizeof(int) * ((size_t)E + 1 + 8 * (size_t)E + (size_t)EP_DISPATCH_WARPS * E);
+    // the limit is set once per device, so to the size of the largest E (1024)
+    static unsigned long long attr_set = 0;
+    const int smem_max = (int)sizeof(int) * (1024 + 1 + 8 * 1024 + EP_DISPATCH_WARPS * 1024);
+    if (!k3_smem_attr(ep_dispatch_kernel, smem_max, attr_set)) return K3MOE_ERR_CUDA;
+    k3_launch(ep_dispatch_kernel, (nch + EP_DISPATCH_WARPS - 1) / EP_DISPATCH_WARPS, 32 * EP_DISPATCH_WARPS, smem, st,
+              idx, T, K, E, R, nch, chunk_cnt, totals, counts + (size_t)src * E, plan->seg, plan->exp_off,
+              plan->exp_seg, plan->info, dest_rank, dest_row, h->d_status);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

@@ -237,37 +237,46 @@ class Layer:
                                   ws.data_ptr(), n, _stream_ptr(stream)), "qb_bias")
         return out
 
-    def ep_plan(self, counts, tokens_per_rank, stream=None):
+    def ep_plan(self, counts, tokens_per_rank, out=None, stream=None):
         """Balanced expert-parallel plan from all ranks' per-expert counts (int32
         CUDA [R, E]) -> dict of int32 CUDA tensors seg [2E, 5] (expert, rank,
-        src, count, dst), rank_seg [R, 2], exp_off [E + 1], exp_seg [2E], info [2]."""
+        src, count, dst), rank_seg [R, 2], exp_off [E + 1], exp_seg [2E], info [2]
+        (written into `out`, such a dict, when given)."""
         import torch
         R, E = counts.shape
         dev = counts.device
-        plan = dict(seg=torch.empty((2 * E, 5), dtype=torch.int32, device=dev),
-                    rank_seg=torch.empty((R, 2), dtype=torch.int32, device=dev),
-                    exp_off=torch.empty(E + 1, dtype=torch.int32, device=dev),
-                    exp_seg=torch.empty(2 * E, dtype=torch.int32, device=dev),
-                    info=torch.empty(2, dtype=torch.int32, device=dev))
+        plan = out if out is not None else dict(
+            seg=torch.empty((2 * E, 5), dtype=torch.int32, device=dev),
+            rank_seg=torch.empty((R, 2), dtype=torch.int32, device=dev),
+            exp_off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            exp_seg=torch.empty(2 * E, dtype=torch.int32, device=dev),
+            info=torch.empty(2, dtype=torch.int32, device=dev))
         check(lib().k3moe_ep_plan_compute(self.h, counts.data_ptr(), R, tokens_per_rank,
                                           C.byref(_ep_struct(plan)), _stream_ptr(stream)), "ep_plan")
         return plan
 
-    def ep_dispatch(self, idx, src_rank, counts, plan, stream=None):
+    def ep_dispatch(self, idx, src_rank, counts, plan, out=None, workspace=None, stream=None):
         """Destinations (rank, row) of source rank src_rank's routed pairs idx
-        (int32 CUDA [S, K]) under `plan` -> two int32 CUDA tensors [S, K]."""
+        (int32 CUDA [S, K]) under `plan` -> two int32 CUDA tensors [S, K]
+        (written into `out`, a pair of such tensors, when given; `workspace` a
+        uint8 CUDA tensor of ep_dispatch_workspace_bytes(S) bytes)."""
         import torch
         S = idx.shape[0]
         n = lib().k3moe_ep_dispatch_workspace_bytes(self.h, S)
         if n == 0:
             raise K3Error(ERR_CODE["ARG"], "ep_dispatch_workspace_bytes")
-        ws = torch.empty(n, dtype=torch.uint8, device=idx.device)
-        rank = torch.empty_like(idx)
-        row = torch.empty_like(idx)
+        if workspace is not None and workspace.numel() >= n:
+            ws, n = workspace, workspace.numel()
+        else:
+            ws = torch.empty(n, dtype=torch.uint8, device=idx.device)
+        rank, row = out if out is not None else (torch.empty_like(idx), torch.empty_like(idx))
         check(lib().k3moe_ep_dispatch(self.h, idx.data_ptr(), S, src_rank, counts.data_ptr(), counts.shape[0],
                                       C.byref(_ep_struct(plan)), rank.data_ptr(), row.data_ptr(), ws.data_ptr(), n,
                                       _stream_ptr(stream)), "ep_dispatch")
         return rank, row
+
+    def ep_dispatch_workspace_bytes(self, tokens_per_rank):
+        return lib().k3moe_ep_dispatch_workspace_bytes(self.h, tokens_per_rank)
 
     def debug_wait_timeout(self, spin_limit, stream=None):
         check(lib().k3moe_debug_wait_timeout(self.h, spin_limit, _stream_ptr(stream)), "wait")

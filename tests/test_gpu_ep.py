@@ -120,7 +120,7 @@ def test_plan_all_load_on_one_expert():
 
 DISPATCH_CASES = [  # E, K, R, S, skew
     (896, 16, 8, 128, 1.2), (896, 16, 4, 1000, 0.0), (896, 16, 2, 40, 2.0), (24, 4, 3, 33, 1.5),
-    (24, 4, 1, 70, 0.0),
+    (24, 4, 1, 70, 0.0), (1024, 8, 16, 64, 1.1),
 ]
 
 
@@ -211,6 +211,11 @@ def test_device_errors_are_reported():
     assert layer.status() == RANGE
     assert plan["info"].cpu().tolist() == [0, -1]
     assert layer.status() == 0                # read and cleared
+    # a dispatch under the failed plan reads none of its other buffers: every pair -1
+    rank, row = layer.ep_dispatch(torch.from_numpy(idx[0]).cuda(), 0, torch.from_numpy(bad.astype(np.int32)).cuda(),
+                                  plan)
+    assert layer.status() == RANGE
+    assert (rank.cpu().numpy() == -1).all() and (row.cpu().numpy() == -1).all()
     plan = _gpu_plan(layer, cnt, S)
     assert layer.status() == 0
     wrong = [i.copy() for i in idx]
