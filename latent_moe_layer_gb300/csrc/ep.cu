@@ -295,11 +295,17 @@ __global__ void __launch_bounds__(32 * EP_DISPATCH_WARPS)
     }
     __syncthreads();
     if (ch >= nch) return;
-    const int t1 = min(T, (ch + 1) * K3_PERM_CHUNK);
-    for (int t = ch * K3_PERM_CHUNK; t < t1; ++t) {
-        if (lane < K) {
-            const int p = t * K + lane;
-            const int e = idx[p];
+    // the chunk's expert ids first (independent loads), then the numbering in
+    // token order from registers
+    const int t0 = ch * K3_PERM_CHUNK, nt = min(T, t0 + K3_PERM_CHUNK) - t0;
+    int ids[K3_PERM_CHUNK];
+#pragma unroll
+    for (int i = 0; i < K3_PERM_CHUNK; ++i) ids[i] = (lane < K && i < nt) ? idx[(size_t)(t0 + i) * K + lane] : -1;
+#pragma unroll
+    for (int i = 0; i < K3_PERM_CHUNK; ++i) {
+        if (i < nt && lane < K) {
+            const int p = (t0 + i) * K + lane;
+            const int e = ids[i];
             int rk = -1, row = -1;
             if (e >= 0 && e < E) {
                 const int j = atomicAdd(&nx[e], 1);     // distinct experts per token: token order
