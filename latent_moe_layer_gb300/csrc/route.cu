@@ -354,15 +354,21 @@ __global__ void __launch_bounds__(32) perm_chunk_scatter_kernel(const int32_t *_
     const int ch = blockIdx.x, lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) next[e] = chunk_base[(size_t)e * nch + ch];
     __syncwarp();
-    const int t1 = min(T, (ch + 1) * K3_PERM_CHUNK);
-    for (int t = ch * K3_PERM_CHUNK; t < t1; ++t) {
-        if (lane < K) {
-            const int p = t * K + lane;
-            const int e = idx[p];
+    // the chunk's expert ids first (independent loads), then the placement in
+    // token order from registers
+    const int t0 = ch * K3_PERM_CHUNK, nt = min(T, t0 + K3_PERM_CHUNK) - t0;
+    int ids[K3_PERM_CHUNK];
+#pragma unroll
+    for (int i = 0; i < K3_PERM_CHUNK; ++i) ids[i] = (lane < K && i < nt) ? idx[(size_t)(t0 + i) * K + lane] : -1;
+#pragma unroll
+    for (int i = 0; i < K3_PERM_CHUNK; ++i) {
+        if (i < nt && lane < K) {
+            const int p = (t0 + i) * K + lane;
+            const int e = ids[i];
             if (e >= 0 && e < E) {                   // the experts of one token are distinct
                 const int row = next[e];
                 next[e] = row + 1;
-                tok_of[row] = t;
+                tok_of[row] = t0 + i;
                 row_of[p] = row;
             }
         }
