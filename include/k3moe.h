@@ -306,7 +306,7 @@ typedef struct {
  * that select expert e (each rank's counts, all-gathered); their sum must be
  * R * S * K and none negative.  tokens_per_rank: S.  n_ranks: R, 1 .. E with
  * E % R == 0 and R * S * K below 2^31.  E up to 1024.
- * One warp on the device; asynchronous on `stream`.  Errors: K3MOE_ERR_ARG
+ * One CTA on the device (its rounds on one warp); asynchronous on `stream`.  Errors: K3MOE_ERR_ARG
  * (NULL pointers, bad sizes), K3MOE_ERR_UNSUPPORTED (E > 1024),
  * K3MOE_ERR_STATE, K3MOE_ERR_CUDA.  Counts that are negative or do not sum to R * S * K are
  * found on the device: the status word gets K3MOE_ERR_RANGE, info gets
