@@ -8,14 +8,19 @@ write) between steps outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
-Default workload: the K3 decode batch of 16 tokens (--config 1).  Under
-torchrun every rank runs an independent replica on its own GPU (the layer is
-token-parallel; no collective on the data path); the time is the max over
-ranks and the value counts the tokens of all ranks.
+Headline workload: the K3 decode batch of 16 tokens (config 1).  Without
+--config the same run then measures the other K3 workloads (decode T=256,
+prefill T=8192, prefill T=32768 with the Zipf selection bias and shared
+experts, and that prefill with a moderate rank-based bias) with the same
+steps, and reports each under detail.configs; --config C measures C alone.
+Under torchrun every rank runs an independent replica on its own GPU (the
+layer is token-parallel; no collective on the data path); the time is the max
+over ranks and the value counts the tokens of all ranks.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -29,10 +34,23 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight GB/s vs HBM peak; prefill TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per touched expert per launch, from the ncu capture in
-# profiles/gemv_expert_decode_dram.md (decode GEMV, 128-expert case, scaled by
-# touched experts).  Valid only while those kernels are unchanged.
-NCU_TRAFFIC_PER_EXPERT = {("gate_up", "gemv"): 12.08e6, ("expert_down", "gemv"): 5.866e6}
+# DRAM bytes (read + write) per touched expert per launch of the decode GEMV,
+# from one ncu capture of a 128-expert case at the K3 shapes, scaled by the
+# touched experts.  They hold for the kernel source whose sha256 prefix is
+# given; any other source reports traffic null until it is captured again.
+NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "a0bf698567dec7b9",
+               "per_expert": {("gate_up", "gemv"): 12.08e6, ("expert_down", "gemv"): 5.866e6}}
+EXTRA_WORKLOADS = [2, 3, 4, "moderate"]
+
+
+def ncu_traffic_per_expert():
+    p = os.path.join(ROOT, NCU_TRAFFIC["source"])
+    try:
+        with open(p, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return {}
+    return NCU_TRAFFIC["per_expert"] if sha == NCU_TRAFFIC["sha256_16"] else {}
 
 
 def peaks():
@@ -154,7 +172,7 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
-def oracle_sample_time(cfg, n_tokens, seed=0, min_seconds=0.0):
+def oracle_sample_time(cfg, n_tokens, seed=0, min_seconds=0.0, dense=None):
     """Time the fp64 oracle on a fixed token sample, repeated until at least
     min_seconds have elapsed; returns (seconds, tokens processed, threads)."""
     import numpy as np
@@ -163,7 +181,7 @@ def oracle_sample_time(cfg, n_tokens, seed=0, min_seconds=0.0):
     rng = np.random.default_rng(1234 + seed)
     rows = np.sort(rng.choice(cfg.T, min(n_tokens, cfg.T), replace=False))
     x = synth.gen_x(cfg, rows)
-    dense = synth.gen_dense(cfg)
+    dense = dense if dense is not None else synth.gen_dense(cfg)
     idx, _, _, _ = oracle.route(cfg, dense, x)
     experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
     t0 = time.perf_counter()
@@ -177,8 +195,9 @@ def oracle_sample_time(cfg, n_tokens, seed=0, min_seconds=0.0):
     return dt, reps * len(rows), oracle.max_threads()
 
 
-def cpu_sample_size(config_id):
-    return {0: 8, 1: 16, 2: 8, 3: 4, 4: 4}.get(config_id, 4)
+def cpu_sample_size(cfg):
+    """Tokens of the oracle's timed sample: the whole batch up to 16 tokens, else 4-8."""
+    return cfg.T if cfg.T <= 16 else (8 if cfg.T <= 256 else 4)
 
 
 # ------------------------------------------------------------------ distributed
@@ -217,16 +236,13 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args):
-    import numpy as np
-    import torch
-    import __graft_entry__ as ge
-    from latent_moe_layer_gb300 import k3moe, synth
-
-    world, rank, local = dist_setup(args.gpus)
-    torch.cuda.set_device(local)
-    ge.build()
-    cfg = synth.CONFIGS[args.config]
+def workload_cfg(key, args=None):
+    """The LayerConfig of a workload key (a config number or "moderate"), with
+    the profiling overrides of args applied when given."""
+    from latent_moe_layer_gb300 import synth
+    cfg = synth.MODERATE_SKEW if key == "moderate" else synth.CONFIGS[key]
+    if args is None:
+        return cfg
     if args.experts:
         # reduced expert count: for profiler captures that must stay a few GB on the device
         cfg = synth.LayerConfig(**{**cfg.__dict__, "E": args.experts, "name": cfg.name + f"_E{args.experts}"})
@@ -236,9 +252,47 @@ def run_ours(args):
         cfg = synth.LayerConfig(**{**cfg.__dict__, "act": args.act, "name": cfg.name + f"_{args.act}"})
     if args.a8:
         cfg = synth.LayerConfig(**{**cfg.__dict__, "a8": True, "name": cfg.name + "_a8"})
-    pk, pk_src = peaks()
+    return cfg
 
-    dw = k3moe.DeviceWeights(cfg)
+
+class WeightCache:
+    """One set of device weights at a time, keyed by everything but the
+    selection bias (the moderate-skew workload reuses config 4's weights with
+    its own bias)."""
+
+    def __init__(self):
+        self.key, self.dw = None, None
+
+    def get(self, cfg):
+        import copy
+        import torch
+        from latent_moe_layer_gb300 import k3moe, synth
+        key = (cfg.wseed, cfg.H, cfg.L, cfg.E, cfg.I, cfg.S, cfg.exp_lo, cfg.exp_hi, cfg.router_dtype,
+               cfg.select_bias)
+        if key != self.key:
+            self.key, self.dw = None, None
+            torch.cuda.empty_cache()
+            self.dw = k3moe.DeviceWeights(cfg)
+            self.key = key
+        dw = self.dw
+        if cfg.select_bias and dw.cfg.bias != cfg.bias:
+            dw = copy.copy(self.dw)
+            dw.cfg = cfg
+            dw.dense = copy.copy(self.dw.dense)
+            dw.dense.select_bias = synth.gen_bias(cfg)
+            dw.bias = torch.from_numpy(dw.dense.select_bias).cuda()
+        return dw
+
+
+def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
+    """Time one workload: W warm-up and K timed steps (L2 flushed before each),
+    then a profiled pass for stage times, the host-buffer e2e, the oracle on a
+    token sample and the training-time extras.  Returns the JSON line's fields."""
+    import numpy as np
+    import torch
+    from latent_moe_layer_gb300 import k3moe, synth
+    world, rank, local, pk, pk_src, flush = (ctx[k] for k in ("world", "rank", "local", "pk", "pk_src",
+                                                              "flush"))
     layer = k3moe.Layer(cfg, path=args.path)
     layer.load(dw)
     path_tensor = layer.path_for(cfg.T) == k3moe.PATH_TENSOR
@@ -248,7 +302,6 @@ def run_ours(args):
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
     wts = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
     ws = layer.workspace(cfg.T)
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
 
     def step():
         layer.forward(xd, out=out, idx_out=idx, w_out=wts, workspace=ws)
@@ -312,10 +365,11 @@ def run_ours(args):
         ach = f / (per_launch_ms / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None}
+                "frac": round(ach / peak, 4), "traffic": None, "peak_kind": "bf16 dense, sustained"}
     key = (dom, "gemv" if (path_tensor and cfg.T * cfg.K <= cfg.E * 24) else "other")
-    if key in NCU_TRAFFIC_PER_EXPERT:
-        roof["traffic"] = round(NCU_TRAFFIC_PER_EXPERT[key] * touched)
+    traffic = ncu_traffic_per_expert()
+    if key in traffic:
+        roof["traffic"] = round(traffic[key] * touched)
         roof["traffic_source"] = "ncu dram bytes per touched expert x touched experts"
     roof.update({"kernel_stage": dom, "per_launch_ms": round(per_launch_ms, 4),
                  "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": pk_src})
@@ -345,95 +399,14 @@ def run_ours(args):
     # CPU baseline: the oracle on a bounded token sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = cpu_sample_size(args.config)
-        dt, nt, thr = oracle_sample_time(cfg, n, min_seconds=10.0)
+        n = cpu_sample_size(cfg)
+        dt, nt, thr = oracle_sample_time(cfg, n, min_seconds=cpu_seconds, dense=dw.dense)
         cpu = {"value": round(nt / dt, 4), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                "sample": f"{n} tokens of {cfg.name} (fp64 oracle, all layer steps), repeated to "
                          f"{nt} tokens in {dt:.2f} s"}
 
-    # Quantile-Balancing bias update (the training-time estimator of the
-    # selection bias), on seeded N(0, 1.5^2) router logits of this workload's shape
-    qb_line = None
-    if cfg.select_bias:
-        g = torch.Generator(device="cuda").manual_seed(7)
-        lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda") * 1.5
-        b0 = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
-        for _ in range(3):
-            layer.qb_bias(lg, b0)
-        # the logits (T E 4 bytes) may fit in L2: flush it before each timed call
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
-        torch.cuda.synchronize()
-        for q0, q1 in ev:
-            flush.zero_()
-            q0.record()
-            layer.qb_bias(lg, b0)
-            q1.record()
-        torch.cuda.synchronize()
-        qms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / len(ev)
-        qbytes = 2 * cfg.T * cfg.E * 4                 # the logits are read twice
-        qb_line = {"ms": round(qms, 4), "algorithmic_bytes": qbytes,
-                   "achieved_gbs": round(qbytes / (qms / 1e3) / 1e9, 1),
-                   "frac": round(qbytes / (qms / 1e3) / 1e9 / pk["hbm_gbs"], 4), "nbins": 1000}
-
-    # Balanced expert-parallel plan and dispatch (the MoonEP step around the
-    # experts), prefill batches only: R ranks each routing this workload's T
-    # tokens (top-K of seeded N(0, 1) logits); one source rank's dispatch timed
-    ep_line = None
-    if cfg.T >= 4096 and not args.no_ep:
-        ep_line = {}
-        g = torch.Generator(device="cuda").manual_seed(9)
-        for R in (8, 64):
-            if cfg.E % R:
-                continue
-            cnt = torch.empty((R, cfg.E), dtype=torch.int32, device="cuda")
-            idx0 = None
-            for q in range(R):
-                lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda")
-                top = torch.topk(lg, cfg.K, dim=1).indices.to(torch.int32).contiguous()
-                cnt[q] = torch.bincount(top.flatten(), minlength=cfg.E).to(torch.int32)
-                if q == 0:
-                    idx0 = top
-            # each call captured once in a CUDA graph with preallocated outputs, so
-            # the events see device time rather than the binding's host overhead
-            plan = layer.ep_plan(cnt, cfg.T)
-            dout = (torch.empty_like(idx0), torch.empty_like(idx0))
-            dws = torch.empty(layer.ep_dispatch_workspace_bytes(cfg.T), dtype=torch.uint8, device="cuda")
-            for _ in range(3):
-                layer.ep_plan(cnt, cfg.T, out=plan)
-                layer.ep_dispatch(idx0, 0, cnt, plan, out=dout, workspace=dws)
-            torch.cuda.synchronize()
-            g_plan, g_disp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_plan):
-                layer.ep_plan(cnt, cfg.T, out=plan)
-            with torch.cuda.graph(g_disp):
-                layer.ep_dispatch(idx0, 0, cnt, plan, out=dout, workspace=dws)
-            n_rep = 20
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
-            torch.cuda.synchronize()
-            for q0, q1 in ev:
-                q0.record()
-                g_plan.replay()
-                q1.record()
-            torch.cuda.synchronize()
-            plan_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
-            for q0, q1 in ev:
-                flush.zero_()
-                q0.record()
-                g_disp.replay()
-                q1.record()
-            torch.cuda.synchronize()
-            disp_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
-            if layer.status() != 0:
-                raise RuntimeError("expert-parallel plan or dispatch reported a device error")
-            info = plan["info"].tolist()
-            pairs = cfg.T * cfg.K
-            dbytes = 12 * pairs                         # idx read, destination rank and row written
-            ep_line[f"ranks_{R}"] = {
-                "tokens_per_rank": cfg.T, "plan_us": round(plan_ms * 1e3, 1), "dispatch_us": round(disp_ms * 1e3, 1),
-                "segments": info[0], "max_redundant_experts": info[1], "redundant_slots_per_rank": cfg.E // R,
-                "dispatch_algorithmic_bytes": dbytes,
-                "dispatch_gbs": round(dbytes / (disp_ms / 1e3) / 1e9, 1), "dispatch_launches": 4,
-                "timing": "CUDA-graph replay of one call, events around the replay"}
+    qb_line = qb_timing(layer, cfg, flush, pk) if (extras and cfg.select_bias) else None
+    ep_line = ep_timing(layer, cfg, flush) if (extras and cfg.T >= 4096 and not args.no_ep) else None
 
     exp_ms = stage_ms["gate_up"] + stage_ms["expert_down"]
     detail = {
@@ -449,19 +422,139 @@ def run_ours(args):
         detail["qb_bias_update"] = qb_line
     if ep_line:
         detail["expert_parallel_plan"] = ep_line
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if path_tensor else "f32", "data": "synthetic",
-        "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
-                   "l2": "flushed between steps (512 MB write, outside the timed events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "weights": "MXFP4 experts (E2M1 + E8M0/32), BF16 dense, seeded synthetic"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": int(round(sum(stage_launch.values()) / max(1, nfw) * args.steps)), "clocks": clk,
-        "detail": detail,
-    }
+    res = {"value": round(value, 2), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
+           "dtype": "f16" if path_tensor else "f32",
+           "config": {"workload": workload_name(cfg), "tokens_per_step": cfg.T,
+                      "l2": "flushed between steps (512 MB write, outside the timed events)",
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "weights": "MXFP4 experts (E2M1 + E8M0/32), BF16 dense, seeded synthetic"},
+           "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+           "gpu_launches": int(round(sum(stage_launch.values()) / max(1, nfw) * args.steps)), "clocks": clk,
+           "detail": detail}
+    del layer, ws
+    return res
+
+
+def qb_timing(layer, cfg, flush, pk):
+    """Quantile-Balancing bias update (the training-time estimator of the
+    selection bias), on seeded N(0, 1.5^2) router logits of this workload's shape."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(7)
+    lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda") * 1.5
+    b0 = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        layer.qb_bias(lg, b0)
+    # the logits (T E 4 bytes) may fit in L2: flush it before each timed call
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    torch.cuda.synchronize()
+    for q0, q1 in ev:
+        flush.zero_()
+        q0.record()
+        layer.qb_bias(lg, b0)
+        q1.record()
+    torch.cuda.synchronize()
+    qms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / len(ev)
+    qbytes = 2 * cfg.T * cfg.E * 4                 # the logits are read twice
+    return {"ms": round(qms, 4), "algorithmic_bytes": qbytes,
+            "achieved_gbs": round(qbytes / (qms / 1e3) / 1e9, 1),
+            "frac": round(qbytes / (qms / 1e3) / 1e9 / pk["hbm_gbs"], 4), "nbins": 1000}
+
+
+def ep_timing(layer, cfg, flush):
+    """Balanced expert-parallel plan and dispatch (the MoonEP step around the
+    experts): R ranks each routing this workload's T tokens (top-K of seeded
+    N(0, 1) logits); one source rank's dispatch timed."""
+    import torch
+    ep_line = {}
+    g = torch.Generator(device="cuda").manual_seed(9)
+    for R in (8, 64):
+        if cfg.E % R:
+            continue
+        cnt = torch.empty((R, cfg.E), dtype=torch.int32, device="cuda")
+        idx0 = None
+        for q in range(R):
+            lg = torch.randn((cfg.T, cfg.E), generator=g, device="cuda")
+            top = torch.topk(lg, cfg.K, dim=1).indices.to(torch.int32).contiguous()
+            cnt[q] = torch.bincount(top.flatten(), minlength=cfg.E).to(torch.int32)
+            if q == 0:
+                idx0 = top
+        # each call captured once in a CUDA graph with preallocated outputs, so
+        # the events see device time rather than the binding's host overhead
+        plan = layer.ep_plan(cnt, cfg.T)
+        dout = (torch.empty_like(idx0), torch.empty_like(idx0))
+        dws = torch.empty(layer.ep_dispatch_workspace_bytes(cfg.T), dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            layer.ep_plan(cnt, cfg.T, out=plan)
+            layer.ep_dispatch(idx0, 0, cnt, plan, out=dout, workspace=dws)
+        torch.cuda.synchronize()
+        g_plan, g_disp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_plan):
+            layer.ep_plan(cnt, cfg.T, out=plan)
+        with torch.cuda.graph(g_disp):
+            layer.ep_dispatch(idx0, 0, cnt, plan, out=dout, workspace=dws)
+        n_rep = 20
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+        torch.cuda.synchronize()
+        for q0, q1 in ev:
+            q0.record()
+            g_plan.replay()
+            q1.record()
+        torch.cuda.synchronize()
+        plan_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
+        for q0, q1 in ev:
+            flush.zero_()
+            q0.record()
+            g_disp.replay()
+            q1.record()
+        torch.cuda.synchronize()
+        disp_ms = sum(q0.elapsed_time(q1) for q0, q1 in ev) / n_rep
+        if layer.status() != 0:
+            raise RuntimeError("expert-parallel plan or dispatch reported a device error")
+        info = plan["info"].tolist()
+        pairs = cfg.T * cfg.K
+        dbytes = 12 * pairs                         # idx read, destination rank and row written
+        ep_line[f"ranks_{R}"] = {
+            "tokens_per_rank": cfg.T, "plan_us": round(plan_ms * 1e3, 1), "dispatch_us": round(disp_ms * 1e3, 1),
+            "segments": info[0], "max_redundant_experts": info[1], "redundant_slots_per_rank": cfg.E // R,
+            "dispatch_algorithmic_bytes": dbytes,
+            "dispatch_gbs": round(dbytes / (disp_ms / 1e3) / 1e9, 1), "dispatch_launches": 4,
+            "timing": "CUDA-graph replay of one call, events around the replay"}
+    return ep_line
+
+
+def run_ours(args):
+    import torch
+    import __graft_entry__ as ge
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    ge.build()
+    pk, pk_src = peaks()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    ctx = dict(world=world, rank=rank, local=local, pk=pk, pk_src=pk_src, flush=flush)
+    cache = WeightCache()
+    head_key = args.config if args.config is not None else 1
+    cfg = workload_cfg(head_key, args)
+    head = measure(cfg, cache.get(cfg), args, ctx, cpu_seconds=10.0)
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+            "data": "synthetic", "config": head["config"], "roofline": head["roofline"],
+            "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"], "detail": head["detail"]}
+    if args.config is None and not args.no_extra:
+        # the other K3 workloads, same steps and warm-up, each with its own
+        # timed region, clocks, roofline and oracle sample
+        configs = {}
+        for key in EXTRA_WORKLOADS:
+            c = workload_cfg(key)
+            r = measure(c, cache.get(c), args, ctx, cpu_seconds=4.0)
+            configs[c.name] = {"workload": r["config"]["workload"], "tokens_per_step": c.T,
+                               "ms_per_step": r["ms_per_step"], "value": r["value"], "unit": r["unit"],
+                               "dtype": r["dtype"], "roofline": r["roofline"], "clocks": r["clocks"],
+                               "cpu_baseline": r["cpu_baseline"], "e2e": r["e2e"],
+                               "gpu_launches": r["gpu_launches"], **r["detail"]}
+        line["detail"]["configs"] = configs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -479,8 +572,8 @@ def run_reference(args):
     from oracle import oracle
     import numpy as np
     oracle.build()
-    cfg = synth.CONFIGS[args.config]
-    n = {1: 2, 2: 2, 3: 1, 4: 1}.get(args.config, 1)
+    cfg = workload_cfg(args.config if args.config is not None else 1)
+    n = 2 if cfg.T <= 256 else 1
     rng = np.random.default_rng(99)
     dense = synth.gen_dense(cfg)
     samples = []
@@ -559,7 +652,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", default=None,
+                    help="measure one workload alone: 0-4 or 'moderate' (default: config 1, then the others)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling aid)")
@@ -570,9 +664,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ep", action="store_true", help="skip the expert-parallel plan timing (prefill configs)")
+    ap.add_argument("--no-extra", action="store_true", help="measure the headline workload only")
     ap.add_argument("--library-peaks", action="store_true",
                     help="print the vendor library's dense BF16 / FP8 / MXFP8 GEMM rates and exit")
     args = ap.parse_args()
+    if args.config is not None and args.config != "moderate":
+        args.config = int(args.config)
     if args.library_peaks:
         library_peaks()
         return

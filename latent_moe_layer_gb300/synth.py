@@ -28,6 +28,11 @@ Recipe (all configurations):
   * shared GLU matrix m, stream (wseed, 6, m): same distributions.
   * selection bias (skewed case), stream (wseed, 7): R_j ~ Zipf(1.1) via
     ``Generator.zipf``, b_j = 2 ln R_j in fp64, stored fp32.
+  * moderate-skew selection bias (bias "rank"), stream (wseed, 7, 1): a seeded
+    permutation gives every expert a rank r_j in 1..E, b_j = -0.25 ln r_j
+    (fp64, stored fp32).  The layer adds its bias to the sigmoid score, so
+    this is the score-space form of a rank-based skew: about a hundred experts
+    receive tokens and the top 16 about two thirds of them.
 """
 from __future__ import annotations
 
@@ -66,6 +71,7 @@ class LayerConfig:
     situ_beta: float = 4.0
     situ_linear_beta: float = 25.0
     a8: bool = False              # MXFP8 activations into the routed experts (the A8 option)
+    bias: str = "zipf"            # selection bias recipe when select_bias: "zipf" or "rank"
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     def with_tokens(self, T: int) -> "LayerConfig":
@@ -101,6 +107,11 @@ CONFIGS = {
     4: LayerConfig("k3_prefill_t32768_skew_shared", seed=4, wseed=4, T=32768, S=6144,
                    select_bias=True, **K3),
 }
+
+# The secondary prefill workload: config 4 (same tokens, weights and shared
+# experts) with the moderate rank-based selection bias instead of the Zipf one.
+MODERATE_SKEW = LayerConfig("k3_prefill_t32768_moderate_skew_shared", seed=4, wseed=4, T=32768, S=6144,
+                            select_bias=True, bias="rank", **K3)
 
 # A small shape whose packed/scale rows are 16-byte aligned (the tensor-core
 # path's requirement) and that spans several 128-row tiles with a ragged tail.
@@ -178,9 +189,16 @@ def gen_gamma(cfg: LayerConfig) -> np.ndarray:
     return np.full(cfg.L, 0x3F80, np.uint16)  # BF16 1.0
 
 
+RANK_BIAS_BETA = 0.25
+
+
 def gen_bias(cfg: LayerConfig) -> np.ndarray | None:
     if not cfg.select_bias:
         return None
+    if cfg.bias == "rank":
+        rank = np.empty(cfg.E, np.float64)
+        rank[_rng(cfg.wseed, _BIAS, 1).permutation(cfg.E)] = np.arange(1, cfg.E + 1)
+        return (-RANK_BIAS_BETA * np.log(rank)).astype(np.float32)
     r = _rng(cfg.wseed, _BIAS).zipf(1.1, cfg.E).astype(np.float64)
     return (2.0 * np.log(r)).astype(np.float32)
 

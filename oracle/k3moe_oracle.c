@@ -112,7 +112,9 @@ double oracle_e4m3(double v)
     double a = fabs(v);
     if (a == 0.0 || isnan(v))
         return v;
-    int e = (int)floor(log2(a));
+    int e;
+    frexp(a, &e);                                /* a = m 2^e, 0.5 <= m < 1: floor(log2 a) = e - 1, exactly */
+    e -= 1;
     if (e < -6)
         e = -6;                                  /* subnormals: spacing stays 2^-9 */
     double step = ldexp(1.0, e - 3);
@@ -135,7 +137,9 @@ void oracle_mxfp8_row(const double *in, int n, double *out)
                 out[32 * b + j] = 0.0;
             continue;
         }
-        int X = (int)floor(log2(amax)) - 8;
+        int X;
+        frexp(amax, &X);                         /* floor(log2 amax) = X - 1, exact (no log2 rounding) */
+        X -= 1 + 8;
         if (X < -127) X = -127;
         if (X > 127) X = 127;
         for (int j = 0; j < 32; j++)

@@ -27,8 +27,8 @@ def e4m3_round(v):
     """Round to the nearest E4M3 value (ties to even), saturating at +-448."""
     v = np.asarray(v, np.float64)
     a = np.abs(v)
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.clip(e, -6, 8)                      # below 2^-6 the spacing stays 2^-9 (subnormals)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))    # a = m 2^e, 0.5 <= m < 1: floor(log2 a) = e - 1
+    e = np.clip(e - 1, -6, 8)                      # below 2^-6 the spacing stays 2^-9 (subnormals)
     step = np.exp2(e - 3)
     q = np.rint(a / step) * step               # numpy rint: ties to even
     q = np.minimum(q, 448.0)
@@ -53,7 +53,7 @@ def mxfp8(x, no_clip=False):
     b = x.reshape(*x.shape[:-1], -1, 32)
     amax = np.abs(b).max(axis=-1, keepdims=True)
     safe = np.where(amax > 0, amax, 1.0)
-    X = np.ceil(np.log2(safe / 448.0)) if no_clip else np.floor(np.log2(safe)) - 8
+    X = np.ceil(np.log2(safe / 448.0)) if no_clip else np.frexp(safe)[1] - 1 - 8
     X = np.clip(X, -127, 127)
     s = np.exp2(X)
     return (e4m3_round(b / s) * s).reshape(x.shape)
@@ -84,6 +84,23 @@ def test_mxfp8_block_scale():
     assert q[41] == 0.3125              # 0.15 -> 10 x 2^-6 (normal, spacing 2^-6), x 2
     assert q[42] == 3 * 2.0 ** -9 * 2   # 0.005 -> 3 x 2^-9 (subnormal), x 2
     assert np.all(q[np.r_[0:3, 4:32]] == 0)
+
+
+def test_mxfp8_scale_one_ulp_below_a_power_of_two():
+    # amax = 2 - 2^-52: floor(log2 amax) = 0, so X = -8 and amax / 2^X = 512 - 2^-44
+    # saturates to 448, giving 1.75.  An exponent taken from a log2 that rounded up
+    # to 1.0 would give X = -7 and 2.0 instead.
+    below = np.nextafter(2.0, 0.0)
+    x = np.zeros(32)
+    x[0], x[1] = below, 0.5
+    for q in (mxfp8(x), oracle.mxfp8(x)):
+        assert q[0] == 1.75 and q[1] == 0.5
+    # the same one ulp below 2^-6 and 2^7: X = -14 and X = -2
+    for amax, want in [(np.nextafter(2.0 ** -6, 0.0), 1.75 * 2.0 ** -7), (np.nextafter(128.0, 0.0), 112.0)]:
+        x[0], x[1] = amax, 0.0
+        for q in (mxfp8(x), oracle.mxfp8(x)):
+            assert q[0] == want, (amax, q[0], want)
+    assert oracle.e4m3(below) == 2.0 and e4m3_round(below) == 2.0
 
 
 # ------------------------------------------------------------------ the layer, re-stated with hooks

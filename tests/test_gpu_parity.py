@@ -5,6 +5,7 @@ sets on every token (or a large sample) and outputs on sampled tokens the
 oracle computes one by one (tokens are independent, so a sample is exact for
 those tokens).
 """
+import copy
 import ctypes as C
 
 import numpy as np
@@ -13,7 +14,8 @@ import pytest
 from latent_moe_layer_gb300 import synth
 from oracle import oracle
 
-from parity_util import assert_parity, compare, device_weights, oracle_rows, run_gpu
+from parity_util import (REPORT, assert_parity, compare, device_weights, index_check, oracle_rows, run_gpu,
+                         selection_gaps)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -164,7 +166,7 @@ def assert_a8_parity(m):
     # most 2^-3 of it).  Such isolated flips can lift single outputs past the 5e-2
     # max-abs bar, so here at most 1e-4 of the outputs may exceed it, none by more
     # than 5x; rel-L2, the indices and the weights keep the full bar.
-    assert m["idx_mismatch"] == 0 and m["w_err"] <= 1e-5, m
+    assert m["idx_mismatch"] == 0 and m["order_bad"] == 0 and m["w_err"] <= 1e-5, m
     assert m["rel_l2"] <= 2e-2, m
     assert m["over_max_abs"] <= max(2, 1e-4 * m["n_out"]) and m["max_abs"] <= 0.25, m
 
@@ -301,58 +303,86 @@ def test_bounded_wait_times_out_and_context_survives():
 
 
 # ------------------------------------------------------------------ K3 sizes
-def _k3_case(cfg_id, n_route, n_out, path=AUTO, seed=0, act="silu", a8=False, check=None):
-    cfg = synth.CONFIGS[cfg_id].with_act(act).with_a8(a8)
-    dw = device_weights(cfg)
+def _k3_case(cfg_id, n_out, path=AUTO, seed=0, act="silu", a8=False, check=None, dw=None):
+    """Index sets and selection order on EVERY token (oracle routing of all T),
+    outputs on n_out sampled tokens (the oracle's full forward of those rows).
+    cfg_id: a config number or a LayerConfig."""
+    base = synth.CONFIGS[cfg_id] if isinstance(cfg_id, int) else cfg_id
+    cfg = base.with_act(act).with_a8(a8)
+    dw = dw if dw is not None else device_weights(cfg)
     g = run_gpu(cfg, path, dw=dw)
     assert g["status"] == 0
     rng = np.random.default_rng(100 + seed)
     T = cfg.T
-    r_rows = np.arange(T) if n_route >= T else np.sort(rng.choice(T, n_route, replace=False))
-    o_rows = r_rows if n_out >= len(r_rows) else np.sort(rng.choice(r_rows, n_out, replace=False))
-    idx, w, gap, _ = oracle.route(cfg, dw.dense, g["x"][r_rows])
-    bad = [i for i, t in enumerate(r_rows)
-           if gap[i] >= 1e-4 and set(g["idx"][t].tolist()) != set(idx[i].tolist())]
-    assert not bad, f"index mismatch on {len(bad)} tokens"
+    idx, w, gap, lg = oracle.route(cfg, dw.dense, g["x"], want_logits=True)
+    ogap = selection_gaps(cfg, dw.dense, idx, lg)
+    del lg
+    set_bad, order_bad, near, n_ordered = index_check(g["idx"], idx, gap, ogap)
+    o_rows = np.arange(T) if n_out >= T else np.sort(rng.choice(T, n_out, replace=False))
     ref = oracle_rows(cfg, dw.dense, g["x"][o_rows])
     m = compare(cfg, g, ref, rows=o_rows)
-    m["near_ties_routed"] = int((gap < 1e-4).sum())
-    print(cfg.name, m)
+    m.update(routed_tokens=T, near_ties_routed=near, order_checked_routed=n_ordered,
+             idx_mismatch_routed=len(set_bad), order_bad_routed=len(order_bad))
+    REPORT.append(f"{cfg.name} path={g['path']} act={act} a8={int(a8)}: tokens {T}, near-ties (gap < 1e-4) "
+                  f"{near}, set mismatches {len(set_bad)}, order checked {n_ordered}, order mismatches "
+                  f"{len(order_bad)}; outputs on {len(o_rows)} tokens: rel-L2 {m['rel_l2']:.3e}, "
+                  f"max-abs {m['max_abs_abs']:.3e} (bound {m['max_abs_bound_abs']:.3e}, output RMS "
+                  f"{m['out_rms']:.3g}), weights {m['w_err']:.2e}")
+    print(REPORT[-1])
+    assert not set_bad, f"index set mismatch on {len(set_bad)} tokens"
+    assert not order_bad, f"selection order mismatch on {len(order_bad)} tokens"
     (check or assert_parity)(m)
     return g, m
 
 
 @pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
 def test_k3_decode_t16(path):
-    g, _ = _k3_case(1, 16, 16, path=path)
+    g, _ = _k3_case(1, 16, path=path)
     assert g["path"] == path
 
 
 def test_k3_decode_t16_situ():
     # the SiTU reading on the decode GEMV at the K3 shapes (weights shared with the SiLU case)
-    _k3_case(1, 16, 16, path=TEN, act="situ")
+    _k3_case(1, 16, path=TEN, act="situ")
 
 
 def test_k3_decode_t16_a8():
-    _k3_case(1, 16, 16, path=TEN, a8=True, check=assert_a8_parity)
+    _k3_case(1, 16, path=TEN, a8=True, check=assert_a8_parity)
 
 
 def test_k3_decode_t256():
-    _k3_case(2, 256, 48)
+    _k3_case(2, 64)
 
 
 @pytest.mark.parametrize("path", [GEN, TEN], ids=["generic", "tensor"])
 def test_k3_prefill_t8192(path):
-    g, _ = _k3_case(3, 512, 24, path=path)
+    g, _ = _k3_case(3, 64, path=path)
     assert g["path"] == path
 
 
 def test_k3_prefill_t32768_skew_shared():
-    g, m = _k3_case(4, 512, 16)
+    g, m = _k3_case(4, 64)
     loads = np.bincount(g["idx"].ravel(), minlength=896)
     assert (loads > 0).sum() < 100            # the Zipf selection bias concentrates the load
     again = run_gpu(synth.CONFIGS[4], AUTO, dw=device_weights(synth.CONFIGS[4]), x=g["x"])
     assert np.array_equal(again["out"], g["out"]) and np.array_equal(again["idx"], g["idx"])
+
+
+def test_k3_prefill_t32768_moderate_skew_shared():
+    # config 4's tokens, weights and shared experts with the moderate rank-based
+    # selection bias: about a hundred experts loaded unevenly (the bias is the
+    # only tensor that differs, so config 4's device weights are reused)
+    base = device_weights(synth.CONFIGS[4])
+    cfg = synth.MODERATE_SKEW
+    dw = copy.copy(base)
+    dw.cfg = cfg
+    dw.dense = copy.copy(base.dense)
+    dw.dense.select_bias = synth.gen_bias(cfg)
+    dw.bias = torch.from_numpy(dw.dense.select_bias).cuda()
+    g, m = _k3_case(cfg, 64, dw=dw)
+    loads = np.bincount(g["idx"].ravel(), minlength=cfg.E)
+    assert 50 < (loads > 0).sum() < 400
+    assert 0.4 < np.sort(loads)[::-1][:16].sum() / loads.sum() < 0.95
 
 
 @pytest.mark.parametrize("cfg_id", [1, 3])

@@ -108,25 +108,59 @@ def test_dequant_consumes_full_row():
 
 
 # ------------------------------------------------------------------ router
-def _tiny():
+# Every router pin runs on both weight types: the tiny case's BF16 router and
+# the fp32 router of the K3 checkpoint (the K3 workloads' branch).
+ROUTERS = ["bf16", "f32"]
+
+
+def _tiny(router_dtype="bf16"):
     cfg = synth.CONFIGS[0]
+    if router_dtype != cfg.router_dtype:
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "router_dtype": router_dtype,
+                                   "name": f"tiny_router_{router_dtype}"})
     dense = synth.gen_dense(cfg)
     x = synth.gen_x(cfg)
     return cfg, dense, x
 
 
-def test_router_logits_against_matmul():
-    cfg, dense, x = _tiny()
+def _router_f64(dense, router_dtype):
+    """W_router widened to fp64 by numpy, independently of the oracle's reader."""
+    if router_dtype == "bf16":
+        assert dense.w_router.dtype == np.uint16
+        return synth.bf16_bits_to_f32(dense.w_router).astype(np.float64)
+    assert dense.w_router.dtype == np.float32
+    return dense.w_router.astype(np.float64)
+
+
+@pytest.mark.parametrize("router_dtype", ROUTERS)
+def test_router_logits_against_matmul(router_dtype):
+    cfg, dense, x = _tiny(router_dtype)
     _, _, _, lg = oracle.route(cfg, dense, x, want_logits=True)
-    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ \
-        synth.bf16_bits_to_f32(dense.w_router).astype(np.float64).T
+    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ _router_f64(dense, router_dtype).T
     np.testing.assert_allclose(lg, ref, rtol=0, atol=1e-12)
 
 
-def test_topk_against_brute_force_subsets():
+def test_fp32_router_logits_at_k3_dimensions():
+    # The K3 router: fp32 W [896, 7168].  The logits equal the fp64 product of the
+    # fp32 weights, and that product is far (> 1e-4) from the product of the same
+    # weights rounded to BF16, so reading the fp32 router at BF16 precision (or its
+    # bytes as BF16 halves) fails this pin.
+    cfg = synth.CONFIGS[1]
+    dense = synth.DenseWeights(synth.gen_router(cfg), None, None, None, None, None)
+    x = synth.gen_x(cfg)[:4]
+    _, _, _, lg = oracle.route(cfg, dense, x, want_logits=True)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    ref = xf @ dense.w_router.astype(np.float64).T
+    np.testing.assert_allclose(lg, ref, rtol=0, atol=1e-12)
+    rounded = xf @ synth.bf16_bits_to_f32(synth.f64_to_bf16_bits(dense.w_router)).astype(np.float64).T
+    assert np.abs(rounded - ref).max() > 1e-4
+
+
+@pytest.mark.parametrize("router_dtype", ROUTERS)
+def test_topk_against_brute_force_subsets(router_dtype):
     # all C(16,4) = 1820 subsets; the selection is the max key-sum subset, and
     # among equal sums the lexicographically lowest (lower index wins ties)
-    cfg, dense, x = _tiny()
+    cfg, dense, x = _tiny(router_dtype)
     rng = np.random.default_rng(7)
     xs = np.concatenate([x, synth.f64_to_bf16_bits(rng.standard_normal((56, cfg.H)))])
     idx, w, gap, lg = oracle.route(cfg, dense, xs, want_logits=True)
@@ -141,8 +175,9 @@ def test_topk_against_brute_force_subsets():
         assert all(lg[t, idx[t, i]] >= lg[t, idx[t, i + 1]] for i in range(cfg.K - 1))
 
 
-def test_ties_go_to_lowest_index():
-    cfg, dense, x = _tiny()
+@pytest.mark.parametrize("router_dtype", ROUTERS)
+def test_ties_go_to_lowest_index(router_dtype):
+    cfg, dense, x = _tiny(router_dtype)
     d = synth.DenseWeights(**dense.__dict__)
     d.w_router = np.tile(dense.w_router[:1], (cfg.E, 1))        # all logits equal
     idx, w, gap, _ = oracle.route(cfg, d, x)
@@ -151,34 +186,38 @@ def test_ties_go_to_lowest_index():
     # one tie at the boundary: rows 9 and 3 equal and top; the lower (3) is taken first
     wr = np.zeros_like(dense.w_router)
     wr[9] = wr[3] = dense.w_router[0]
-    d.w_router = wr
     xs = np.abs(synth.bf16_bits_to_f32(x)).astype(np.float64)
     xpos = synth.f64_to_bf16_bits(xs)
     dpos = synth.DenseWeights(**d.__dict__)
-    dpos.w_router = synth.f64_to_bf16_bits(np.abs(synth.bf16_bits_to_f32(wr)))
+    if router_dtype == "bf16":
+        dpos.w_router = synth.f64_to_bf16_bits(np.abs(synth.bf16_bits_to_f32(wr)))
+    else:
+        dpos.w_router = np.abs(wr)
     idx, _, _, _ = oracle.route(cfg, dpos, xpos)
     assert np.all(idx[:, 0] == 3) and np.all(idx[:, 1] == 9)
     # rest are zero logits: lowest remaining indices
     assert np.all(idx[:, 2] == 0) and np.all(idx[:, 3] == 1)
 
 
-def test_weights_sum_to_one_and_match_sigmoid():
-    cfg, dense, x = _tiny()
+@pytest.mark.parametrize("router_dtype", ROUTERS)
+def test_weights_sum_to_one_and_match_sigmoid(router_dtype):
+    cfg, dense, x = _tiny(router_dtype)
     idx, w, gap, lg = oracle.route(cfg, dense, x, want_logits=True)
     np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-12)
     s = 1 / (1 + np.exp(-np.take_along_axis(lg, idx, 1)))
     np.testing.assert_allclose(w, s / s.sum(1, keepdims=True), rtol=1e-14)
 
 
-def test_bias_selects_but_never_weights():
-    cfg = synth.CONFIGS[0]
+@pytest.mark.parametrize("router_dtype", ROUTERS)
+def test_bias_selects_but_never_weights(router_dtype):
+    cfg, dense, x = _tiny(router_dtype)
     cfgb = synth.LayerConfig(**{**cfg.__dict__, "select_bias": True})
-    dense = synth.gen_dense(cfg)
-    x = synth.gen_x(cfg)
     rng = np.random.default_rng(5)
     b = rng.standard_normal(cfg.E).astype(np.float32)
     db = synth.DenseWeights(**{**dense.__dict__, "select_bias": b})
     idx, w, gap, lg = oracle.route(cfgb, db, x, want_logits=True)
+    np.testing.assert_allclose(lg, synth.bf16_bits_to_f32(x).astype(np.float64) @
+                               _router_f64(dense, router_dtype).T, rtol=0, atol=1e-12)
     s = 1 / (1 + np.exp(-lg))
     key = s + b.astype(np.float64)
     for t in range(x.shape[0]):

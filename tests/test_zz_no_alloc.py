@@ -2,10 +2,12 @@
 
 It serves callers that cannot allocate device memory (plugin hosts that give
 an operator only its input and output buffers): its logits scratch is a static
-device array inside the library.  Checked through the C ABI against the
-routing that k3moe_forward returns, on two calls in a row with different
-inputs, so a stale scratch from the first call would show in the second.
-This file is collected last on purpose.
+device array inside the library.  Checked through the C ABI, on two calls in a
+row with different inputs (a stale scratch from the first call would show in
+the second), against the routing that k3moe_forward returns and against the
+fp64 oracle under the parity rule (index sets and order where the key gaps are
+>= 1e-4, weights within 1e-5); and the device memory in use must not change
+across calls after the first.  This file is collected last on purpose.
 """
 import ctypes as C
 
@@ -13,6 +15,7 @@ import numpy as np
 import pytest
 
 from latent_moe_layer_gb300 import synth
+from oracle import oracle
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -21,6 +24,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 from latent_moe_layer_gb300 import k3moe  # noqa: E402
+from parity_util import GAP, index_check, selection_gaps  # noqa: E402
 
 W_TOL = 1e-5          # the mixture-weight tolerance of the parity tests
 MAX_LOGITS = 256 * 1024
@@ -70,14 +74,35 @@ def test_route_static_matches_forward_two_calls(cfg):
         w = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
         layer.forward(x, idx_out=idx, w_out=w)
         refs.append((x, idx.cpu().numpy(), w.cpu().numpy()))
+    outs = [(torch.empty((T, cfg.K), dtype=torch.int32, device="cuda"),
+             torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")) for T, _ in calls]
+    # a first call on this device resolves the static array's address; from
+    # then on the calls must leave the device's memory use unchanged
+    for (T, _), (x, _, _), (idx, w) in zip(calls, refs, outs):
+        assert _route_static(layer, x, T, idx, w) == 0
     torch.cuda.synchronize()
-    for (T, _), (x, ridx, rw) in zip(calls, refs):
-        idx = torch.full((T, cfg.K), -1, dtype=torch.int32, device="cuda")
-        w = torch.full((T, cfg.K), -1.0, dtype=torch.float32, device="cuda")
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for (T, _), (x, ridx, rw), (idx, w) in zip(calls, refs, outs):
+        idx.fill_(-1)
+        w.fill_(-1.0)
         assert _route_static(layer, x, T, idx, w) == 0
         torch.cuda.synchronize()
-        assert np.array_equal(idx.cpu().numpy(), ridx)
-        assert np.abs(w.cpu().numpy() - rw).max() <= W_TOL
+        assert torch.cuda.mem_get_info()[0] == free0 and torch.cuda.memory_allocated() == alloc0
+        g_idx, g_w = idx.cpu().numpy(), w.cpu().numpy()
+        # against the oracle: the parity rule on index sets, order and weights
+        x_np = x.cpu().numpy().view(np.uint16)
+        o_idx, o_w, gap, lg = oracle.route(cfg, dense, x_np, want_logits=True)
+        set_bad, order_bad, _, _ = index_check(g_idx, o_idx, gap, selection_gaps(cfg, dense, o_idx, lg))
+        assert not set_bad and not order_bad, (set_bad, order_bad)
+        for t in np.nonzero(gap >= GAP)[0]:
+            pos = {int(e): k for k, e in enumerate(o_idx[t])}
+            assert max(abs(g_w[t, k] - o_w[t, pos[int(e)]]) for k, e in enumerate(g_idx[t])) <= W_TOL
+        # and the forward's routing on the same tokens (same rule: the two logit
+        # paths differ by about 1e-6, so only near-ties may differ)
+        f_bad, f_order, _, _ = index_check(g_idx, ridx, gap, selection_gaps(cfg, dense, o_idx, lg))
+        assert not f_bad and not f_order
+        keep = gap >= GAP
+        assert np.abs(g_w[keep] - rw[keep]).max() <= W_TOL
     assert layer.status() == 0
 
 
