@@ -647,6 +647,25 @@ def library_peaks(steps=50):
     print(json.dumps(out))
 
 
+def mma_peaks(iters=4096):
+    """The tensor cores' own rate for each MMA kind the expert GEMMs use: back-to-back
+    tcgen05.mma on shared-memory operands, one CTA per SM (k3moe_mma_peak).  Prints
+    one JSON line of TFLOP/s; the block-scaled A8 roofline divides by the E2M1 x E4M3
+    figure at N = 224, the tile width of the block-scaled expert GEMMs."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    from latent_moe_layer_gb300 import k3moe
+    out = {"method": "tcgen05.mma back to back, M 128, operands in shared memory, one CTA per SM, "
+                     f"{iters} x 128 K per CTA, CUDA events"}
+    for kind, ns in [("f16", (256, 224)), ("mxf8f6f4_e4m3", (256, 224)), ("mxf8f6f4_e2m1_e4m3", (256, 224, 192))]:
+        for n in ns:
+            k3moe.mma_peak(kind, n, iters // 8)        # warm the clocks
+            out[f"{kind}_n{n}_tflops"] = round(k3moe.mma_peak(kind, n, iters), 1)
+    out["device"] = torch.cuda.get_device_name(0)
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -665,6 +684,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ep", action="store_true", help="skip the expert-parallel plan timing (prefill configs)")
     ap.add_argument("--no-extra", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--mma-peaks", action="store_true",
+                    help="print the tensor cores' own MMA rates (tcgen05 microbenchmark) and exit")
     ap.add_argument("--library-peaks", action="store_true",
                     help="print the vendor library's dense BF16 / FP8 / MXFP8 GEMM rates and exit")
     args = ap.parse_args()
@@ -672,6 +693,9 @@ def main():
         args.config = int(args.config)
     if args.library_peaks:
         library_peaks()
+        return
+    if args.mma_peaks:
+        mma_peaks()
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -372,6 +372,16 @@ int k3moe_debug_dequant(const uint8_t *packed, const uint8_t *scale, int rows, i
  * status word and returns; read it with k3moe_status(). */
 int k3moe_debug_wait_timeout(k3moe_handle *h, int spin_limit, cudaStream_t stream);
 
+/* Tensor-core peak microbenchmark (the roofline denominator of the expert GEMMs):
+ * one CTA per SM issues `iters` x 128 K of back-to-back tcgen05.mma, M = 128 and
+ * N = n (16..256, a multiple of 16), on operands resident in shared memory.
+ * kind 0: kind::f16 (f16 x f16); 1: kind::mxf8f6f4 E4M3 x E4M3; 2: kind::mxf8f6f4
+ * E2M1 x E4M3 (the A8 expert GEMMs' operands), both with E8M0 block scales.
+ * Writes the launch's milliseconds to *ms (CUDA events on `stream`; synchronises);
+ * its work is SMs x iters x 2 x 128 x n x 128 flops.  A timed-out wait is recorded in
+ * status[0] (device int32[4], caller-owned). */
+int k3moe_mma_peak(int kind, int n, int iters, int *status, float *ms, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -237,6 +237,14 @@ int k3moe_load_weights(k3moe_handle *h, const k3moe_weights *w, void *persistent
         al = al && c.hidden % 512 == 0 && c.shared_inter % 512 == 0;
         for (int i = 0; i < 6; ++i) al = al && ((uintptr_t)sh[i] % 16 == 0);
     }
+    // A8: the block-scaled expert GEMMs read the packed FP4 rows through TMA's
+    // unpacking type, which needs 32-byte aligned bases and row strides
+    if (c.a8) {
+        al = al && c.latent % 64 == 0 && c.inter % 64 == 0;
+        for (int i = 0; i < 6 && al; i += 2)
+            for (int e = 0; e < c.n_experts; ++e)
+                if ((uintptr_t)tabs[i][e] % 32) { al = false; break; }
+    }
     if (c.path == K3MOE_PATH_TENSOR && !al) return K3MOE_ERR_ALIGN;
 
     K3_CUDA_TRY(cudaGetDevice(&h->device));
@@ -341,6 +349,7 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->chunk_cnt = cv.take<int32_t>(T >= K3_PERM_CHUNKED_T
                                          ? (size_t)c.n_experts * ((T + K3_PERM_CHUNK - 1) / K3_PERM_CHUNK)
                                          : 1);
+    ws->mxs = cv.take<uint8_t>(c.a8 ? R * (size_t)(c.latent + c.inter) / 32 + 16 : 1);
     ws->bytes = align_up(cv.off, 256);
     return K3MOE_OK;
 }

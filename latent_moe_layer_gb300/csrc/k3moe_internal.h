@@ -260,6 +260,7 @@ struct k3_ws {
     int32_t *stage_idx;   // [T, K]
     float *stage_w;       // [T, K]
     int32_t *chunk_cnt;   // [E, ceil(T / K3_PERM_CHUNK)] per-chunk counts, then bases (large T)
+    uint8_t *mxs;         // A8: E8M0 scales of the MXFP8 expert inputs, [T*K, L/32] then [T*K, I/32]
     size_t bytes;
 };
 

@@ -95,6 +95,46 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// The same box written to the same shared-memory offset of every CTA of the
+// cluster in `mask`, each CTA's mbarrier at `bar`'s offset receiving the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int c0, int c1,
+                                               uint16_t mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ncluster_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -177,6 +217,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
         : "memory");
 }
 
+// The same, arriving on `bar`'s offset in every CTA of the cluster in `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -238,6 +287,56 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, int bf16)
     d |= (uint32_t)(N >> 3) << 17;
     d |= (uint32_t)(M >> 4) << 24;
     return d;
+}
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb)^T, kind::mxf8f6f4 with one E8M0 scale per
+// 32 K values of each operand row (scale_vec::1X): A and B from shared-memory
+// descriptors (8-bit elements, or 4-bit E2M1 unpacked to 16-byte groups as the
+// 16U4_ALIGN16B TMA type lays them), K = 32 per instruction.  Scale factors in TMEM:
+// A row m at lane m, column sfa_tmem + m / 32; B row n at lane 32 q + n % 32 of every
+// lane quarter q (the quarter of the D rows that read it), column sfb_tmem + n / 32;
+// the byte of the 32-bit cell is the scale-factor id of the instruction descriptor.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: B scale-factor id in bits 4-5,
+// A / B element type in bits 7-9 / 10-12 (0 = E4M3, 5 = E2M1), both K-major, N >> 3 in
+// bits 17-22, scale type UE8M0 (bit 23 = 1), M >> 4 in bits 24-28, A scale-factor id in
+// bits 29-30.
+constexpr uint32_t MX_E4M3 = 0, MX_E2M1 = 5;
+__host__ __device__ __forceinline__ uint32_t idesc_mx(int M, int N, uint32_t atype, uint32_t btype, int sfa_id,
+                                                      int sfb_id)
+{
+    uint32_t d = 0;
+    d |= (uint32_t)(sfb_id & 3) << 4;
+    d |= (atype & 7u) << 7;
+    d |= (btype & 7u) << 10;
+    d |= (uint32_t)(N >> 3) << 17;
+    d |= 1u << 23;
+    d |= (uint32_t)(M >> 4) << 24;
+    d |= (uint32_t)(sfa_id & 3) << 29;
+    return d;
+}
+
+// 32 lanes x 32 bit, 1 / 8 consecutive columns: thread i of the warp writes lane (base + i).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 // Hardware tanh approximation (PTX tanh.approx.f32; relative error about 2^-11),

@@ -8,6 +8,7 @@
 #include "tc_expert.cuh"
 #include "gemv_expert.h"
 #include "dense_tc.h"
+#include "mx_expert.h"
 
 using namespace k3;
 
@@ -184,7 +185,14 @@ int pick_bn(int T, int K, int E)
 
 bool k3_tc_available() { return encode_fn() != nullptr; }
 
-size_t k3_tc_tmap_count(const k3moe_config &c) { return (size_t)3 * c.n_experts + 3; }
+// [w1, w3, w2] per expert, the shared experts' three; with the A8 option also the
+// block-scaled GEMMs' FP4 weight maps [w1, w3, w2] per expert, then their scale maps.
+size_t k3_tc_tmap_count(const k3moe_config &c) { return (size_t)3 * c.n_experts + 3 + (c.a8 ? (size_t)6 * c.n_experts : 0); }
+
+namespace k3 {
+bool k3_encode_mx_weight(CUtensorMap *m, const void *packed, int rows, int cols);
+bool k3_encode_mx_scale(CUtensorMap *m, const void *scale, int rows, int cols);
+}
 
 size_t k3_tc_hilo_bytes(const k3moe_config &c)
 {
@@ -213,6 +221,19 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
         if (!encode_packed(&maps[3 * E + 0], h->shared[0], S, H)) return K3MOE_ERR_CUDA;
         if (!encode_packed(&maps[3 * E + 1], h->shared[2], S, H)) return K3MOE_ERR_CUDA;
         if (!encode_packed(&maps[3 * E + 2], h->shared[4], H, S)) return K3MOE_ERR_CUDA;
+    }
+    if (c.a8) {
+        // block-scaled expert GEMMs: FP4 weights unpacked by TMA, and their scale bytes
+        CUtensorMap *mw = maps.data() + 3 * E + 3, *ms = mw + 3 * E;
+        for (int e = 0; e < E; ++e) {
+            if (!k3_encode_mx_weight(&mw[3 * e + 0], tabs[0][e], I, L) ||
+                !k3_encode_mx_weight(&mw[3 * e + 1], tabs[2][e], I, L) ||
+                !k3_encode_mx_weight(&mw[3 * e + 2], tabs[4][e], L, I) ||
+                !k3_encode_mx_scale(&ms[3 * e + 0], tabs[1][e], I, L) ||
+                !k3_encode_mx_scale(&ms[3 * e + 1], tabs[3][e], I, L) ||
+                !k3_encode_mx_scale(&ms[3 * e + 2], tabs[5][e], L, I))
+                return K3MOE_ERR_CUDA;
+        }
     }
     K3_CUDA_TRY(cudaMemcpyAsync(h->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap),
                                 cudaMemcpyHostToDevice, st));
@@ -454,20 +475,134 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
     return rc;
 }
 
-int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws &ws, cudaStream_t st)
+// Combine + RMSNorm, the up-projection and the shared experts (after the routed
+// experts have written y [R, L] BF16).
+static int finish_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws &ws, cudaStream_t st)
 {
     const k3moe_config &c = h->cfg;
     const int H = c.hidden, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter, S = c.shared_inter;
+    const uint8_t *rm = h->d_rowmax;
+    int rc;
+    {
+        k3_stage sg(h, K3MOE_STAGE_COMBINE, st);
+        if ((rc = k3_launch_combine_norm(ws.y, 1, ws.row_of, ws.wts, h->gamma, T, K, L, c.rms_eps, ws.nrm, st)))
+            return rc;
+    }
+    {
+        k3_stage sg(h, K3MOE_STAGE_UP, st);
+        if ((rc = dense_up(h, T, ws, S > 0 ? nullptr : (uint16_t *)out, st))) return rc;
+    }
+    if (S == 0) return K3MOE_OK;                 // the up-projection wrote the BF16 output
+    if (S > 0) {
+        const int sbn = T <= 64 ? 32 : 256;
+        int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
+        {
+            k3_stage sg(h, K3MOE_STAGE_PREP, st);
+            k3_launch(prep_f16_rows_kernel, T, 256, 0, st, (const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
+                                                    ws.xscale);
+            k3_note_launch();
+            k3_launch(dense_tiles_kernel, 1, 256, 0, st, T, sbn, stiles, ws.meta + 2);
+            k3_note_launch();
+            K3_CUDA_TRY(cudaGetLastError());
+        }
+        ActMaps sb1, sb2;
+        if (!encode_act_maps(&sb1, ws.xs, T, H) || !encode_act_maps(&sb2, ws.sact, T, S)) return K3MOE_ERR_CUDA;
+        const uint8_t *rs = rm + (size_t)E * (2 * I + L);
+        ExpertGemmArgs s1 = {};
+        s1.a8 = 0;                                   // the shared experts stay A16
+        s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;
+        s1.amap_stride = 3;
+        s1.amap_off[0] = 0;
+        s1.amap_off[1] = 1;
+        s1.status = h->d_status;
+        s1.spin_limit = 0xFFFFFFFFu;
+        s1.scales[0] = k3_shared_tab(h, 1);
+        s1.scales[1] = k3_shared_tab(h, 3);
+        s1.rowmax[0] = rs;
+        s1.rowmax[1] = rs + S;
+        s1.rows = S;
+        s1.K = H;
+        s1.tiles = stiles;
+        s1.n_tiles = ws.meta + 2;
+        s1.rscale = ws.xscale;
+        s1.act = k3_act_of(c);
+        s1.out = ws.sact;
+        ExpertGemmArgs s2 = s1;
+        s2.amap_off[0] = s2.amap_off[1] = 2;
+        s2.scales[0] = s2.scales[1] = k3_shared_tab(h, 5);
+        s2.rowmax[0] = s2.rowmax[1] = rs + 2 * S;
+        s2.rows = H;
+        s2.K = S;
+        s2.rscale = nullptr;
+        s2.addend = ws.o32;                          // the up-projection's fp32 output
+        s2.out = out;                                // BF16 layer output = up + shared, rounded once
+        const int nt = (T + sbn - 1) / sbn;
+        if ((rc = expert_pair(h, sbn, sb1, sb2, s1, s2, nt * (S / EX_BM), nt * (H / EX_BM), st,
+                              K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED_DOWN, true)))
+            return rc;
+    }
+    return K3MOE_OK;
+}
+
+int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws &ws, cudaStream_t st)
+{
+    const k3moe_config &c = h->cfg;
+    const int L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
     const int R = T * K;
-    const int bn = pick_bn(T, K, E);
+    const bool gemv = pick_bn(T, K, E) == 32;   // routed experts at decode sizes: the streaming GEMV
+    const bool mx = c.a8 && !gemv;              // A8 at tile sizes: block-scaled MXFP4 x MXFP8 MMAs
+    const int bn = mx ? MX_BN : pick_bn(T, K, E);
     int rc;
     if ((rc = dense_router_down(h, x, T, ws, st))) return rc;
-    // A8: the routed experts read h as MXFP8 (rounded in place from its BF16 value)
-    if (c.a8 && (rc = k3_launch_mx8_rows(ws.h, 0, ws.h, 0, (size_t)T * L, h->d_status, h->num_sms, st)))
+    // A8 through the decode GEMV: the routed experts read h as MXFP8 (rounded in place
+    // from its BF16 value); the block-scaled path quantises h in its own prep
+    if (c.a8 && gemv && (rc = k3_launch_mx8_rows(ws.h, 0, ws.h, 0, (size_t)T * L, h->d_status, h->num_sms, st)))
         return rc;
-    const bool gemv = bn == 32;     // routed experts at decode sizes: the streaming GEMV
     // top-K and the permutation; token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
     if ((rc = k3_launch_route(h, ws, T, gemv ? 16 : bn, st))) return rc;
+    const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
+    if (mx) {
+        // h as MXFP8 in expert order [R, L] (+ scales), the GLU output as MXFP8 [R, I] (+ scales)
+        uint8_t *hq8 = (uint8_t *)ws.hperm, *aq8 = hq8 + (size_t)R * L;
+        uint8_t *hs8 = ws.mxs, *as8 = hs8 + (size_t)R * (L / 32);
+        {
+            k3_stage sg(h, K3MOE_STAGE_PREP, st);
+            if ((rc = k3_launch_prep_mx8(ws.h, T, L, ws.row_of, K, hq8, hs8, h->num_sms, st))) return rc;
+        }
+        MxActMaps mb1, mb2;
+        if (!k3_encode_mx_act(&mb1, hq8, hs8, R, L) || !k3_encode_mx_act(&mb2, aq8, as8, R, I)) return K3MOE_ERR_CUDA;
+        MxGemmArgs m1 = {};
+        m1.wmaps = (const CUtensorMap *)h->d_tmaps + 3 * E + 3;
+        m1.smaps = m1.wmaps + 3 * E;
+        m1.map_stride = 3;
+        m1.map_off[0] = 0;
+        m1.map_off[1] = 1;
+        m1.rows = I;
+        m1.K = L;
+        m1.tiles = (const int4 *)ws.tiles;
+        m1.n_tiles = ws.meta + 1;
+        m1.out_q = aq8;
+        m1.out_s = as8;
+        m1.status = h->d_status;
+        m1.spin_limit = 0xFFFFFFFFu;
+        m1.act = k3_act_of(c);
+        MxGemmArgs m2 = m1;
+        m2.map_off[0] = m2.map_off[1] = 2;
+        m2.rows = L;
+        m2.K = I;
+        m2.out_q = nullptr;
+        m2.out_s = nullptr;
+        m2.out_bf16 = (uint16_t *)ws.y;
+        {
+            k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
+            if ((rc = k3_launch_mx_expert(MX_GLU, mb1, m1, max_ntiles * (I / 64), h->num_sms, st))) return rc;
+        }
+        {
+            k3_stage sg(h, K3MOE_STAGE_EXPERT_DOWN, st);
+            if ((rc = k3_launch_mx_expert(MX_DOWN, mb2, m2, max_ntiles * (L / 128), h->num_sms, st))) return rc;
+        }
+        return finish_tc(h, x, T, out, ws, st);
+    }
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
         k3_launch(prep_f16_rows_kernel, dim3(T, prep_split(T, K, h->num_sms)), 256, 0, st, ws.h, L, ws.row_of, K,
@@ -475,7 +610,6 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
-    const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
     ActMaps bm1, bm2;
     // the down projection's f16 input: the GLU output (MXFP8-rounded in the tcgen05 epilogue
     // with A8), or for the decode GEMV with A8 its rounding from fp32 (in hperm)
@@ -558,59 +692,5 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
                                  st, K3MOE_STAGE_GATE_UP, K3MOE_STAGE_EXPERT_DOWN, false))) {
         return rc;
     }
-    {
-        k3_stage sg(h, K3MOE_STAGE_COMBINE, st);
-        if ((rc = k3_launch_combine_norm(ws.y, 1, ws.row_of, ws.wts, h->gamma, T, K, L, c.rms_eps, ws.nrm, st)))
-            return rc;
-    }
-    {
-        k3_stage sg(h, K3MOE_STAGE_UP, st);
-        if ((rc = dense_up(h, T, ws, S > 0 ? nullptr : (uint16_t *)out, st))) return rc;
-    }
-    if (S == 0) return K3MOE_OK;                 // the up-projection wrote the BF16 output
-    if (S > 0) {
-        const int sbn = T <= 64 ? 32 : 256;
-        int4 *stiles = (int4 *)ws.tiles;            // the routed tile list is no longer needed
-        {
-            k3_stage sg(h, K3MOE_STAGE_PREP, st);
-            k3_launch(prep_f16_rows_kernel, T, 256, 0, st, (const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
-                                                    ws.xscale);
-            k3_note_launch();
-            k3_launch(dense_tiles_kernel, 1, 256, 0, st, T, sbn, stiles, ws.meta + 2);
-            k3_note_launch();
-            K3_CUDA_TRY(cudaGetLastError());
-        }
-        ActMaps sb1, sb2;
-        if (!encode_act_maps(&sb1, ws.xs, T, H) || !encode_act_maps(&sb2, ws.sact, T, S)) return K3MOE_ERR_CUDA;
-        const uint8_t *rs = rm + (size_t)E * (2 * I + L);
-        ExpertGemmArgs s1 = a1;
-        s1.a8 = 0;                                   // the shared experts stay A16
-        s1.amaps = (const CUtensorMap *)h->d_tmaps + (size_t)3 * E;
-        s1.amap_stride = 3;
-        s1.scales[0] = k3_shared_tab(h, 1);
-        s1.scales[1] = k3_shared_tab(h, 3);
-        s1.rowmax[0] = rs;
-        s1.rowmax[1] = rs + S;
-        s1.rows = S;
-        s1.K = H;
-        s1.tiles = stiles;
-        s1.n_tiles = ws.meta + 2;
-        s1.rscale = ws.xscale;
-        s1.act = k3_act_of(c);
-        s1.out = ws.sact;
-        ExpertGemmArgs s2 = s1;
-        s2.amap_off[0] = s2.amap_off[1] = 2;
-        s2.scales[0] = s2.scales[1] = k3_shared_tab(h, 5);
-        s2.rowmax[0] = s2.rowmax[1] = rs + 2 * S;
-        s2.rows = H;
-        s2.K = S;
-        s2.rscale = nullptr;
-        s2.addend = ws.o32;                          // the up-projection's fp32 output
-        s2.out = out;                                // BF16 layer output = up + shared, rounded once
-        const int nt = (T + sbn - 1) / sbn;
-        if ((rc = expert_pair(h, sbn, sb1, sb2, s1, s2, nt * (S / EX_BM), nt * (H / EX_BM), st,
-                              K3MOE_STAGE_SHARED, K3MOE_STAGE_SHARED_DOWN, true)))
-            return rc;
-    }
-    return K3MOE_OK;
+    return finish_tc(h, x, T, out, ws, st);
 }

@@ -26,7 +26,8 @@ EXPORTS = ["k3moe_create", "k3moe_persistent_bytes", "k3moe_load_weights", "k3mo
            "k3moe_forward", "k3moe_forward_host", "k3moe_status", "k3moe_destroy", "k3moe_strerror",
            "k3moe_path_for", "k3moe_debug_dequant", "k3moe_debug_wait_timeout",
            "k3moe_profile_enable", "k3moe_profile_read", "k3moe_stage_name", "k3moe_qb_workspace_bytes",
-           "k3moe_qb_bias", "k3moe_ep_plan_compute", "k3moe_ep_dispatch_workspace_bytes", "k3moe_ep_dispatch"]
+           "k3moe_qb_bias", "k3moe_ep_plan_compute", "k3moe_ep_dispatch_workspace_bytes", "k3moe_ep_dispatch",
+           "k3moe_route_static", "k3moe_mma_peak"]
 STAGES = ["router", "down_proj", "topk", "permute", "gate_up", "expert_down", "combine_norm",
           "up_proj", "shared", "finish", "prep", "shared_down"]
 
@@ -102,6 +103,8 @@ def lib():
         L.k3moe_ep_dispatch_workspace_bytes.argtypes = [vp, i]
         L.k3moe_ep_dispatch_workspace_bytes.restype = sz
         L.k3moe_ep_dispatch.argtypes = [vp, vp, i, i, vp, i, C.POINTER(EpPlan), vp, vp, vp, sz, vp]
+        L.k3moe_route_static.argtypes = [vp, vp, i, vp, vp, vp]
+        L.k3moe_mma_peak.argtypes = [i, i, i, vp, C.POINTER(C.c_float), vp]
         for name in EXPORTS:
             getattr(L, name)
         _lib = L
@@ -280,6 +283,22 @@ class Layer:
 
     def debug_wait_timeout(self, spin_limit, stream=None):
         check(lib().k3moe_debug_wait_timeout(self.h, spin_limit, _stream_ptr(stream)), "wait")
+
+
+MMA_KINDS = {"f16": 0, "mxf8f6f4_e4m3": 1, "mxf8f6f4_e2m1_e4m3": 2}
+
+
+def mma_peak(kind, n=256, iters=4096, stream=None):
+    """TFLOP/s of back-to-back tcgen05.mma of `kind` (a MMA_KINDS key), M 128, N n, on all SMs."""
+    import torch
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ms = C.c_float()
+    check(lib().k3moe_mma_peak(MMA_KINDS[kind], n, iters, status.data_ptr(), C.byref(ms), _stream_ptr(stream)),
+          "mma_peak")
+    if int(status[0]) != 0:
+        raise K3Error(int(status[0]), "mma_peak")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * iters * 2.0 * 128 * n * 128 / (ms.value * 1e-3) / 1e12
 
 
 def _ep_struct(plan):

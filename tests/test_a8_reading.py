@@ -189,3 +189,47 @@ def test_oracle_a8_mode_is_the_restated_layer():
                             quant_h=lambda v: mxfp8(_bf16_round(v)))
     assert _rel_l2(a8["out"], re) < 1e-12
     assert 2e-2 < _rel_l2(a8["out"], exact["out"]) < 1e-1
+
+
+def test_a8_output_moves_with_one_bf16_ulp_of_h():
+    # Reading 16 quantises h from its BF16 value.  A BF16 h value that lies on an
+    # E4M3 rounding tie (1 in 16 of them) changes its E4M3 code by a full step when
+    # h moves by one BF16 ulp, and the GLU output's own MXFP8 rounding turns the
+    # resulting ~0.1-0.5% shift of the gate/up sums into a percent-level change of
+    # the token's output.  An implementation whose BF16 h differs from the exactly
+    # rounded one in a few elements per token (fp32 instead of fp64 accumulation)
+    # therefore lands percent-level away on some tokens: the A8 parity bar allows
+    # those outputs past max-abs (at most 1e-3 of them, none past 0.25) while
+    # rel-L2 keeps the full bar.  The A16 layer moves by orders of magnitude less.
+    cfg = synth.SMALL_ALIGNED.with_tokens(4)
+    dense = synth.gen_dense(cfg)
+    x = synth.gen_x(cfg)
+    idx, _, _, _ = oracle.route(cfg, dense, x)
+    experts = {int(e): synth.gen_expert(cfg, int(e)) for e in np.unique(idx)}
+    ref = oracle.forward(cfg, dense, experts, x, want_latent=True)
+    hb = _bf16_round(ref["h"])
+    t = 0
+    # an element of token 0 on an E4M3 tie, not its block's maximum
+    q = mxfp8(hb[t:t + 1])[0]
+    tie = None
+    for j in range(cfg.L):
+        blk = slice(32 * (j // 32), 32 * (j // 32) + 32)
+        if abs(hb[t, j]) >= np.abs(hb[t, blk]).max():
+            continue
+        up = hb[t, j] + 2.0 ** (np.frexp(abs(hb[t, j]))[1] - 8)     # the next BF16 value up
+        h2 = hb[t].copy()
+        h2[j] = up
+        if mxfp8(h2[None])[0][j] != q[j] and abs(hb[t, j]) > 0.5:
+            tie = (j, up)
+            break
+    assert tie is not None
+    j, up = tie
+    h_pert = hb.copy()
+    h_pert[t, j] = up
+    a8_base = _layer_from_latent(cfg, dense, experts, hb, ref["idx"], ref["w"], mxfp8)
+    a8_pert = _layer_from_latent(cfg, dense, experts, h_pert, ref["idx"], ref["w"], mxfp8)
+    a16_base = _layer_from_latent(cfg, dense, experts, hb, ref["idx"], ref["w"], lambda v: v)
+    a16_pert = _layer_from_latent(cfg, dense, experts, h_pert, ref["idx"], ref["w"], lambda v: v)
+    d8 = np.linalg.norm(a8_pert[t] - a8_base[t]) / np.linalg.norm(a8_base[t])
+    d16 = np.linalg.norm(a16_pert[t] - a16_base[t]) / np.linalg.norm(a16_base[t])
+    assert d8 > 1e-3 and d8 > 20 * d16, (d8, d16)

@@ -160,15 +160,19 @@ def test_situ_parity(path, name, T):
 
 
 def assert_a8_parity(m):
-    # The MXFP8 rounding decisions are taken on the kernel's fp32 values and on the
-    # oracle's fp64 values: an activation within about 1e-6 (relative) of an E4M3
-    # tie can round the other way, moving that one element by one E4M3 step (at
-    # most 2^-3 of it).  Such isolated flips can lift single outputs past the 5e-2
-    # max-abs bar, so here at most 1e-4 of the outputs may exceed it, none by more
-    # than 5x; rel-L2, the indices and the weights keep the full bar.
+    # The MXFP8 rounding decisions are taken on the kernel's values and on the
+    # oracle's: h is rounded to BF16 from an fp32 (tensor-core) sum on the GPU and
+    # from the fp64 sum in the oracle, so a few BF16 h values per token differ by
+    # one ulp, and one in sixteen of those sits on an E4M3 tie and takes the other
+    # code; the GLU output's own MXFP8 rounding amplifies that into a change of
+    # about a percent of the token's output (pinned on the oracle alone in
+    # test_a8_reading.py::test_a8_output_moves_with_one_bf16_ulp_of_h); the fp32
+    # GLU values flip isolated E4M3 codes the same way.  So here at most 1e-3 of the
+    # outputs may exceed the 5e-2 max-abs bar, none by more than 5x; rel-L2, the
+    # indices, their order and the weights keep the full bar.
     assert m["idx_mismatch"] == 0 and m["order_bad"] == 0 and m["w_err"] <= 1e-5, m
     assert m["rel_l2"] <= 2e-2, m
-    assert m["over_max_abs"] <= max(2, 1e-4 * m["n_out"]) and m["max_abs"] <= 0.25, m
+    assert m["over_max_abs"] <= max(2, 1e-3 * m["n_out"]) and m["max_abs"] <= 0.25, m
 
 
 # The A8 option (MXFP8 h and GLU output into the routed experts) against the
@@ -348,6 +352,22 @@ def test_k3_decode_t16_situ():
 
 def test_k3_decode_t16_a8():
     _k3_case(1, 16, path=TEN, a8=True, check=assert_a8_parity)
+
+
+def test_k3_prefill_t8192_a8():
+    # the block-scaled MXFP4 x MXFP8 expert GEMMs at the K3 prefill shape
+    g, _ = _k3_case(3, 64, path=TEN, a8=True, check=assert_a8_parity)
+    assert g["path"] == TEN
+
+
+@pytest.mark.parametrize("T", [300, 1500])
+def test_a8_situ_block_scaled(T):
+    # the SiTU reading in the block-scaled GLU epilogue
+    cfg = synth.SMALL_ALIGNED.with_tokens(T).with_a8().with_act("situ")
+    g = run_gpu(cfg, TEN)
+    assert g["status"] == 0
+    ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_a8_parity(compare(cfg, g, ref))
 
 
 def test_k3_decode_t256():
