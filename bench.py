@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # given; any other source reports traffic null until it is captured again.
 NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "a0bf698567dec7b9",
                "per_expert": {("gate_up", "gemv"): 12.08e6, ("expert_down", "gemv"): 5.866e6}}
-EXTRA_WORKLOADS = [2, 3, 4, "moderate"]
+EXTRA_WORKLOADS = [2, 3, 4, "moderate", "3a8"]
 
 
 def ncu_traffic_per_expert():
@@ -240,7 +240,11 @@ def workload_cfg(key, args=None):
     """The LayerConfig of a workload key (a config number or "moderate"), with
     the profiling overrides of args applied when given."""
     from latent_moe_layer_gb300 import synth
-    cfg = synth.MODERATE_SKEW if key == "moderate" else synth.CONFIGS[key]
+    if key == "3a8":            # the T=8192 prefill with MXFP8 activations (block-scaled expert GEMMs)
+        cfg = synth.CONFIGS[3].with_a8(True)
+        cfg = synth.LayerConfig(**{**cfg.__dict__, "name": cfg.name + "_a8"})
+    else:
+        cfg = synth.MODERATE_SKEW if key == "moderate" else synth.CONFIGS[key]
     if args is None:
         return cfg
     if args.experts:
@@ -361,6 +365,13 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
         ach = b / (per_launch_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None}
+    elif getattr(cfg, "a8", False) and dom in ("gate_up", "expert_down") and ctx.get("mma_peaks"):
+        # block-scaled kind::mxf8f6f4 expert GEMMs: the tensor cores' own rate for that kind
+        ach = f / (per_launch_ms / 1e3) / 1e12
+        peak = ctx["mma_peaks"]["mxf8f6f4_e2m1_e4m3_n224_tflops"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": None,
+                "peak_kind": "tcgen05 kind::mxf8f6f4 E2M1 x E4M3, N 224, own microbenchmark (burst)"}
     else:
         ach = f / (per_launch_ms / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
@@ -372,7 +383,8 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
         roof["traffic"] = round(traffic[key] * touched)
         roof["traffic_source"] = "ncu dram bytes per touched expert x touched experts"
     roof.update({"kernel_stage": dom, "per_launch_ms": round(per_launch_ms, 4),
-                 "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": pk_src})
+                 "algorithmic_bytes": b, "algorithmic_flops": f,
+                 "peak_source": "own microbenchmark" if "own" in roof.get("peak_kind", "") else pk_src})
 
     # end to end through the host-buffer C-ABI call
     e2e = None
@@ -532,6 +544,8 @@ def run_ours(args):
     pk, pk_src = peaks()
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
     ctx = dict(world=world, rank=rank, local=local, pk=pk, pk_src=pk_src, flush=flush)
+    if args.config is None or getattr(args, "a8", False) or args.config == "3a8":
+        ctx["mma_peaks"] = measure_mma_peaks()
     cache = WeightCache()
     head_key = args.config if args.config is not None else 1
     cfg = workload_cfg(head_key, args)
@@ -555,6 +569,8 @@ def run_ours(args):
                                "cpu_baseline": r["cpu_baseline"], "e2e": r["e2e"],
                                "gpu_launches": r["gpu_launches"], **r["detail"]}
         line["detail"]["configs"] = configs
+    if ctx.get("mma_peaks"):
+        line["detail"]["mma_peaks"] = ctx["mma_peaks"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -647,6 +663,18 @@ def library_peaks(steps=50):
     print(json.dumps(out))
 
 
+def measure_mma_peaks(iters=4096):
+    """TFLOP/s of back-to-back tcgen05.mma per kind (k3moe_mma_peak), one CTA per SM."""
+    from latent_moe_layer_gb300 import k3moe
+    out = {"method": "tcgen05.mma back to back, M 128, operands in shared memory, one CTA per SM, "
+                     f"{iters} x 128 K per CTA, CUDA events"}
+    for kind, ns in [("f16", (256, 224)), ("mxf8f6f4_e4m3", (256, 224)), ("mxf8f6f4_e2m1_e4m3", (256, 224, 192))]:
+        for n in ns:
+            k3moe.mma_peak(kind, n, iters // 8)        # warm the clocks
+            out[f"{kind}_n{n}_tflops"] = round(k3moe.mma_peak(kind, n, iters), 1)
+    return out
+
+
 def mma_peaks(iters=4096):
     """The tensor cores' own rate for each MMA kind the expert GEMMs use: back-to-back
     tcgen05.mma on shared-memory operands, one CTA per SM (k3moe_mma_peak).  Prints
@@ -655,13 +683,7 @@ def mma_peaks(iters=4096):
     import torch
     import __graft_entry__ as ge
     ge.build()
-    from latent_moe_layer_gb300 import k3moe
-    out = {"method": "tcgen05.mma back to back, M 128, operands in shared memory, one CTA per SM, "
-                     f"{iters} x 128 K per CTA, CUDA events"}
-    for kind, ns in [("f16", (256, 224)), ("mxf8f6f4_e4m3", (256, 224)), ("mxf8f6f4_e2m1_e4m3", (256, 224, 192))]:
-        for n in ns:
-            k3moe.mma_peak(kind, n, iters // 8)        # warm the clocks
-            out[f"{kind}_n{n}_tflops"] = round(k3moe.mma_peak(kind, n, iters), 1)
+    out = measure_mma_peaks(iters)
     out["device"] = torch.cuda.get_device_name(0)
     print(json.dumps(out))
 
@@ -672,7 +694,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=None,
-                    help="measure one workload alone: 0-4 or 'moderate' (default: config 1, then the others)")
+                    help="measure one workload alone: 0-4, 'moderate' or '3a8' (default: config 1, then the others)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 generic, 2 tensor")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling aid)")
@@ -689,7 +711,7 @@ def main():
     ap.add_argument("--library-peaks", action="store_true",
                     help="print the vendor library's dense BF16 / FP8 / MXFP8 GEMM rates and exit")
     args = ap.parse_args()
-    if args.config is not None and args.config != "moderate":
+    if args.config is not None and args.config not in ("moderate", "3a8"):
         args.config = int(args.config)
     if args.library_peaks:
         library_peaks()

@@ -68,6 +68,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
     uint16_t *hilo = cv.take<uint16_t>(k3_tc_hilo_bytes(c) / 2 + 1);
     int *flag = cv.take<int>(1);
     (void)flag;
+    float *glu_bound = cv.take<float>(4);
     if (h) {
         h->d_status = st;
         for (int i = 0; i < 6; ++i) h->d_eptr[i] = tabs[i];
@@ -76,6 +77,7 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
         h->tmap_count = ntm;
         h->d_rowmax = rmax;
         h->d_router_hilo = hilo;
+        h->d_glu_bound = glu_bound;
     }
     return align_up(cv.off, 256);
 }
@@ -331,6 +333,7 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     // f16 expert inputs: the permuted h; with A8 also the MXFP8 GLU output [R, I]
     ws->hperm = cv.take<uint16_t>(R * (c.latent > c.inter ? c.latent : c.inter) + 1);
     ws->hscale = cv.take<float>(R + 1);
+    ws->ascale = cv.take<float>(R + 1);
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
     ws->o32 = cv.take<float>(Tn * c.hidden);
     {   // split-K partials for the decode-size dense GEMMs: up to K3_DENSE_MAX_SPLITS splits
@@ -342,6 +345,7 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->sact = cv.take<float>(c.shared_inter ? Tn * c.shared_inter : 1);
     ws->xs = cv.take<uint16_t>(c.shared_inter ? Tn * c.hidden : 1);
     ws->xscale = cv.take<float>(Tn);
+    ws->xascale = cv.take<float>(Tn);
     ws->stage_x = cv.take<uint16_t>(Tn * c.hidden);
     ws->stage_out = cv.take<uint16_t>(Tn * c.hidden);
     ws->stage_idx = cv.take<int32_t>(R + 1);

@@ -271,12 +271,14 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                             if (a.out_f32) {
                                 reinterpret_cast<float *>(a.out)[orow * a.rows + row] = av;
                             } else {
-                                if (!(fabsf(av) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
-                                reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(av);
+                                // an exact power of two keeps |a| inside the f16 range
+                                const float as = a.ascale ? av * pow2_inverse(__ldg(a.ascale + orow)) : av;
+                                if (!(fabsf(as) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
+                                reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(as);
                             }
                         } else {
-                            reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] =
-                                f32_to_bf16(acc[0][nb][q]);
+                            const float y = a.ascale ? acc[0][nb][q] * __ldg(a.ascale + orow) : acc[0][nb][q];
+                            reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] = f32_to_bf16(y);
                         }
                     }
                 }

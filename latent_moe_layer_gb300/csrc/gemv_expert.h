@@ -17,6 +17,8 @@ struct GemvArgs {
     const int4 *tiles;                 // (group, first B row, B rows <= 16) per token tile
     const int *n_tiles;                // device count of tiles
     const float *rscale;               // [R] per-row factor applied to the GLU inputs, or nullptr
+    const float *ascale;               // [R] per-row power of two 2^k: the f16 GLU output is divided by it,
+                                       // the down projection's output multiplied by it; or nullptr
     K3Act act;                         // GLU activation
     int out_f32;                       // GLU: 1 writes fp32 [R, rows] (the A8 path rounds it afterwards)
     void *out;                         // GLU: f16 (or fp32) [R, rows]; BF16: BF16 [R, rows]

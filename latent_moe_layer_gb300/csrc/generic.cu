@@ -395,7 +395,8 @@ template <> __device__ __forceinline__ float mx8_load<float>(const float *p) { r
 // out_kind: 0 BF16, 1 fp32, 2 f16 (|q| > 65504 is reported as K3MOE_ERR_RANGE)
 template <typename TI>
 __global__ void __launch_bounds__(256) mx8_rows_kernel(const TI *__restrict__ in, void *__restrict__ out,
-                                                       int out_kind, size_t nblk, int *status)
+                                                       int out_kind, size_t nblk, int *status,
+                                                       const float *__restrict__ row_div, int row_len)
 {
     griddep_enter();
     const int lane = threadIdx.x & 31;
@@ -411,8 +412,10 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const TI *__restrict__ in
         if (out_kind == 0) reinterpret_cast<uint16_t *>(out)[i] = f32_to_bf16(q);
         else if (out_kind == 1) reinterpret_cast<float *>(out)[i] = q;
         else {
-            if (!(fabsf(q) <= 65504.f)) set_status(status, K3MOE_ERR_RANGE, 4);
-            reinterpret_cast<__half *>(out)[i] = __float2half_rn(q);
+            // f16 output: divided by its row's power of two (exact) to stay inside the f16 range
+            const float qs = row_div ? q * pow2_inverse(row_div[i / row_len]) : q;
+            if (!(fabsf(qs) <= 65504.f)) set_status(status, K3MOE_ERR_RANGE, 4);
+            reinterpret_cast<__half *>(out)[i] = __float2half_rn(qs);
         }
     }
 }
@@ -506,16 +509,18 @@ int k3_launch_wait_debug(int *status, int spin_limit, cudaStream_t st)
 }
 
 int k3_launch_mx8_rows(const void *in, int in_fp32, void *out, int out_kind, size_t n, int *status, int num_sms,
-                       cudaStream_t st)
+                       cudaStream_t st, const float *row_div, int row_len)
 {
     if (n == 0) return K3MOE_OK;
     if (n % 32) return K3MOE_ERR_SHAPE;
     const size_t nblk = n / 32;
     const unsigned grid = (unsigned)std::min<size_t>((nblk + 7) / 8, (size_t)8 * (num_sms > 0 ? num_sms : 148));
     if (in_fp32)
-        k3_launch(mx8_rows_kernel<float>, grid, 256, 0, st, (const float *)in, out, out_kind, nblk, status);
+        k3_launch(mx8_rows_kernel<float>, grid, 256, 0, st, (const float *)in, out, out_kind, nblk, status, row_div,
+                  row_len);
     else
-        k3_launch(mx8_rows_kernel<uint16_t>, grid, 256, 0, st, (const uint16_t *)in, out, out_kind, nblk, status);
+        k3_launch(mx8_rows_kernel<uint16_t>, grid, 256, 0, st, (const uint16_t *)in, out, out_kind, nblk, status,
+                  row_div, row_len);
     k3_note_launch();
     return K3_LAUNCH_OK();
 }

@@ -90,6 +90,12 @@ __device__ __forceinline__ float mx8_round(float v, float amax)
     return mx8_round_x(v, mx8_scale_exp((__float_as_uint(amax) >> 23) & 0xFF));
 }
 
+// 2^-k for a power of two 2^k with 0 <= k <= 126 (exact: exponent arithmetic).
+__device__ __forceinline__ float pow2_inverse(float p2)
+{
+    return __uint_as_float(0x7F000000u - (__float_as_uint(p2) & 0x7F800000u));
+}
+
 // 2^(e-127) for an E8M0 byte e in [0, 254] (e = 0 gives the fp32 subnormal 2^-127).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e)
 {
@@ -202,6 +208,7 @@ struct k3moe_handle {
     void *d_tmaps = nullptr;                   // tensor-path TMA descriptors (CUtensorMap[])
     uint8_t *d_rowmax = nullptr;               // tensor-path per-row max exponent bytes
     uint16_t *d_router_hilo = nullptr;         // tensor-path router weights as BF16 [E, 2H] (hi | lo)
+    float *d_glu_bound = nullptr;              // largest gate / up row L2 norms: routed w1, w3, shared ws1, ws3
     size_t tmap_count = 0;
     k3_prof *prof = nullptr;                   // stage timing, when enabled
     // split-K plans of the decode-size dense GEMMs per token count (0 = not planned yet):
@@ -248,6 +255,8 @@ struct k3_ws {
     void *y;              // [T*K, L] fp32 (generic) or BF16 (tensor path)
     void *hperm;          // [T*K, L] f16 (tensor path) activation rows in expert order
     float *hscale;        // [T*K] per-row power-of-two factor of hperm
+    float *ascale;        // [T*K] per-row power of two 2^k the f16 GLU output is divided by (the down projection multiplies it back)
+    float *xascale;       // [T] the same for the shared experts' GLU output
     uint16_t *nrm;        // [T, L] BF16 normalised latent
     float *o32;           // [T, H] fp32 up_proj output (generic path: + shared; tensor path: the shared down's addend)
     float *part;          // split-K partials of the dense tensor-core GEMMs (small T only)
@@ -296,10 +305,11 @@ int k3_launch_route(k3moe_handle *h, const k3_ws &ws, int T, int tile_n, cudaStr
 int k3_launch_rows_gemm(const void *A, int a_bf16, int M, int K, const void *W, int w_bf16, int N,
                         float *out_f32, uint16_t *out_bf16, int accumulate, cudaStream_t st);
 // A8: n values (n a multiple of 32; blocks of 32 along rows) rounded to OCP MXFP8;
-// in BF16 (in_fp32 = 0) or fp32; out_kind 0 BF16, 1 fp32, 2 f16.  in may equal out
+// in BF16 (in_fp32 = 0) or fp32; out_kind 0 BF16, 1 fp32, 2 f16 (divided by the power
+// of two row_div[i / row_len] of its row when row_div is given).  in may equal out
 // when the element sizes match.
 int k3_launch_mx8_rows(const void *in, int in_fp32, void *out, int out_kind, size_t n, int *status, int num_sms,
-                       cudaStream_t st);
+                       cudaStream_t st, const float *row_div = nullptr, int row_len = 1);
 int k3_launch_glu_generic(const k3::K3Act &act_fn, const uint16_t *in, int din, const int32_t *row_token, int rows,
                           const uint8_t *const *w1p, const uint8_t *const *w1s,
                           const uint8_t *const *w3p, const uint8_t *const *w3s,

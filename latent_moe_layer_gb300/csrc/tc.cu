@@ -81,11 +81,17 @@ __global__ void rowmax_kernel(const uint8_t *const *tab, int groups, int rows, i
 // One CTA per token: amax of the BF16 row, power-of-two factor 2^k with
 // amax * 2^k in [2^14, 2^15), f16 copies of the scaled row to each permuted row
 // of the token (row_of[t*K + k]) or to row t (row_of == nullptr), and the
-// inverse factor 2^-k per written row.
+// inverse factor 2^-k per written row.  With `bound` (bound[0] bound[1] >= the
+// largest gate row norm times the largest up row norm of the GLU this row feeds)
+// it also writes ascale[row] = 2^j, the smallest power of two with
+// bound ||h||^2 2^-j <= 2^15: the GLU output |silu(g) u| <= |g| |u| <= bound ||h||^2
+// divided by 2^j is inside the f16 range whatever the token's scale.
 __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__restrict__ src, int cols,
                                                            const int32_t *__restrict__ row_of, int K,
                                                            __half *__restrict__ dst,
-                                                           float *__restrict__ rscale)
+                                                           float *__restrict__ rscale,
+                                                           const float *__restrict__ bound,
+                                                           float *__restrict__ ascale)
 {
     griddep_enter();
     const int t = blockIdx.x, tid = threadIdx.x;
@@ -117,6 +123,36 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
     }
     const float up = __uint_as_float((uint32_t)(k + 127) << 23);
     const float down = __uint_as_float((uint32_t)(127 - k) << 23);
+    float a_fac = 1.f;
+    if (bound) {
+        // S = sum (h 2^k)^2 (each term < 2^30), ||h||^2 = S 2^-2k
+        float ss = 0.f;
+        for (int i = tid * 8; i < cols; i += 256 * 8) {
+            uint4 v = *reinterpret_cast<const uint4 *>(s + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = __uint_as_float(w[q] << 16) * up, hi = __uint_as_float(w[q] & 0xffff0000u) * up;
+                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+            }
+        }
+        __syncthreads();                    // red[] is reused
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) ss += red[w];
+        const float c = bound[0] * bound[1];
+        if (ss > 0.f && c > 0.f) {
+            int ec, es;
+            frexpf(c, &ec);
+            frexpf(ss, &es);                // log2(c S 2^-2k) < ec + es - 2k
+            const int j = max(0, min(126, ec + es - 2 * k - 15));
+            a_fac = __uint_as_float((uint32_t)(j + 127) << 23);
+        }
+    }
     for (int kk = blockIdx.y; kk < K; kk += gridDim.y) {     // this CTA's copies of the row
         const int row = row_of ? row_of[(size_t)t * K + kk] : t;
         __half *d = dst + (size_t)row * cols;
@@ -133,8 +169,45 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
             }
             *reinterpret_cast<uint4 *>(d + i) = o;
         }
-        if (tid == 0) rscale[row] = down;
+        if (tid == 0) {
+            rscale[row] = down;
+            if (ascale) ascale[row] = a_fac;
+        }
     }
+}
+
+// Largest row L2 norm of dequantised MXFP4 matrices [rows, K] (one per group), as a
+// float atomically maxed into *out (bit pattern of a non-negative float): the
+// E2M1 magnitudes squared per 32-value block (exact in fp32) times 2^(2(e - 127)),
+// summed in fp64.
+__global__ void row_norm_max_kernel(const uint8_t *const *ptab, const uint8_t *const *stab, int rows, int K,
+                                    unsigned int *out)
+{
+    const int g = blockIdx.y;
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    float n = 0.f;
+    if (r < rows) {
+        const uint8_t *p = ptab[g] + (size_t)r * (K / 2);
+        const uint8_t *sc = stab[g] + (size_t)r * (K / 32);
+        double acc = 0.0;
+        for (int b = 0; b < K / 32; ++b) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(p + 16 * b);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float sq = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float m = e2m1_to_f32((w[q] >> (4 * c)) & 0xFu, 1.f);
+                    sq = fmaf(m, m, sq);
+                }
+            acc += ldexp((double)sq, 2 * ((int)sc[b] - 127));
+        }
+        n = (float)fmin(sqrt(acc), 3.0e38);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n = fmaxf(n, __shfl_xor_sync(0xffffffffu, n, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(n));
 }
 
 // CTAs per token for prep_f16_rows_kernel: the K copies of a row are spread
@@ -251,6 +324,17 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
     if (c.router_dtype == K3MOE_ROUTER_F32) {
         int rc = k3_launch_split_hilo((const float *)h->w_router, E, H, h->d_router_hilo, st);
         if (rc) return rc;
+    }
+    // bounds of the GLU outputs: largest gate and up row norms [routed w1, w3, shared ws1, ws3]
+    unsigned int *nb = (unsigned int *)h->d_glu_bound;
+    K3_CUDA_TRY(cudaMemsetAsync(nb, 0, 4 * sizeof(float), st));
+    row_norm_max_kernel<<<dim3((I + 127) / 128, E), 128, 0, st>>>(h->d_eptr[0], h->d_eptr[1], I, L, nb);
+    row_norm_max_kernel<<<dim3((I + 127) / 128, E), 128, 0, st>>>(h->d_eptr[2], h->d_eptr[3], I, L, nb + 1);
+    if (S > 0) {
+        row_norm_max_kernel<<<dim3((S + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 0), k3_shared_tab(h, 1), S, H,
+                                                                       nb + 2);
+        row_norm_max_kernel<<<dim3((S + 127) / 128, 1), 128, 0, st>>>(k3_shared_tab(h, 2), k3_shared_tab(h, 3), S, H,
+                                                                       nb + 3);
     }
     K3_CUDA_TRY(cudaGetLastError());
     return K3MOE_OK;
@@ -499,7 +583,7 @@ static int finish_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_
         {
             k3_stage sg(h, K3MOE_STAGE_PREP, st);
             k3_launch(prep_f16_rows_kernel, T, 256, 0, st, (const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
-                                                    ws.xscale);
+                      ws.xscale, c.act == K3MOE_ACT_SITU ? nullptr : (const float *)h->d_glu_bound + 2, ws.xascale);
             k3_note_launch();
             k3_launch(dense_tiles_kernel, 1, 256, 0, st, T, sbn, stiles, ws.meta + 2);
             k3_note_launch();
@@ -525,6 +609,7 @@ static int finish_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_
         s1.tiles = stiles;
         s1.n_tiles = ws.meta + 2;
         s1.rscale = ws.xscale;
+        s1.ascale = ws.xascale;
         s1.act = k3_act_of(c);
         s1.out = ws.sact;
         ExpertGemmArgs s2 = s1;
@@ -533,7 +618,8 @@ static int finish_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_
         s2.rowmax[0] = s2.rowmax[1] = rs + 2 * S;
         s2.rows = H;
         s2.K = S;
-        s2.rscale = nullptr;
+        s2.rscale = ws.xascale;
+        s2.ascale = nullptr;
         s2.addend = ws.o32;                          // the up-projection's fp32 output
         s2.out = out;                                // BF16 layer output = up + shared, rounded once
         const int nt = (T + sbn - 1) / sbn;
@@ -605,8 +691,11 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     }
     {
         k3_stage sg(h, K3MOE_STAGE_PREP, st);
+        // the GLU output's power-of-two divisor (SiTU outputs are bounded by 100 and need none); A8
+        // through the GEMV keeps the GLU output in fp32 until its MXFP8 rounding, which applies it
         k3_launch(prep_f16_rows_kernel, dim3(T, prep_split(T, K, h->num_sms)), 256, 0, st, ws.h, L, ws.row_of, K,
-                  (__half *)ws.hperm, ws.hscale);
+                  (__half *)ws.hperm, ws.hscale, c.act == K3MOE_ACT_SITU ? nullptr : (const float *)h->d_glu_bound,
+                  ws.ascale);
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
@@ -630,6 +719,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a1.tiles = (const int4 *)ws.tiles;
     a1.n_tiles = ws.meta + 1;
     a1.rscale = ws.hscale;
+    a1.ascale = ws.ascale;                       // GLU output divided by 2^k ...
     a1.act = k3_act_of(c);
     a1.out = ws.act;
     a1.a8 = c.a8;                                // MXFP8 rounding fused in the GLU epilogue
@@ -642,7 +732,8 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     a2.rowmax[0] = a2.rowmax[1] = rm + (size_t)2 * E * I;
     a2.rows = L;
     a2.K = I;
-    a2.rscale = nullptr;
+    a2.rscale = ws.ascale;                       // ... and the down projection's output multiplied by it
+    a2.ascale = nullptr;
     a2.out = ws.y;
     if (gemv) {
         // few tokens per expert: streaming GEMV, FP4 decoded in registers
@@ -658,6 +749,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g1.tiles = (const int4 *)ws.tiles;
         g1.n_tiles = ws.meta + 1;
         g1.rscale = ws.hscale;
+        g1.ascale = c.a8 ? nullptr : ws.ascale;  // A8: fp32 GLU output, the factor applied in its rounding
         g1.act = k3_act_of(c);
         g1.out = ws.act;
         g1.out_f32 = c.a8;
@@ -669,6 +761,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g2.rows = L;
         g2.K = I;
         g2.rscale = nullptr;
+        g2.ascale = ws.ascale;
         g2.out = ws.y;
         {
             k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
@@ -678,7 +771,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
                 return rc;
             // A8: the GLU output (fp32) rounded to MXFP8, as the down projection's f16 input
             if (c.a8 && (rc = k3_launch_mx8_rows(ws.act, 1, ws.hperm, 2, (size_t)R * I, h->d_status, h->num_sms,
-                                                 st)))
+                                                 st, ws.ascale, I)))
                 return rc;
         }
         {

@@ -44,7 +44,8 @@ struct ExpertGemmArgs {
     int K;                           // reduction length (multiple of 512)
     const int4 *tiles;               // (group, row0, nrows, -) per token tile
     const int *n_tiles;              // device count of tiles
-    const float *rscale;             // per B-row factor (GLU input scaling) or nullptr
+    const float *rscale;             // per B-row factor: GLU, of the inputs (h scaling); other modes, of the outputs; or nullptr
+    const float *ascale;             // GLU: per B-row power of two 2^k the f16 output is divided by, or nullptr
     void *out;                       // GLU: f16 [R, rows]; BF16 and BF16_ADD: BF16 [R, rows]
     const float *addend;             // BF16_ADD: fp32 [R, rows] added before the rounding to BF16
     int *status;
@@ -80,7 +81,7 @@ struct ExpertSmem {
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
     static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
     static constexpr int OFF_RS = (OFF_BAR + N_BAR * 8 + 16 + 15) & ~15;   // after the tmem holder and abort flag; 16-byte reads
-    static constexpr int BYTES = OFF_RS + BN * 4 + 1024;              // + per-token factors + align slack
+    static constexpr int BYTES = OFF_RS + BN * 4 + BN + 1024;         // + per-token factors and exponents + align slack
 };
 
 __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
@@ -445,12 +446,18 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             const int acc = (int)(tc % NACC);
             const float fw0 = e8m0_to_f32(__ldg(args.rowmax[0] + (size_t)g * args.rows + row));
             const float fw1 = NMAT == 2 ? e8m0_to_f32(__ldg(args.rowmax[NMAT - 1] + (size_t)g * args.rows + row1)) : 0.f;
-            if (MODE == OUT_GLU_F16) {
-                // the tile's per-token factors, staged while its MMAs run, once
-                // the epilogue warps have finished with the previous tile's
+            {
+                // the tile's per-token factors, staged while its MMAs run, once the
+                // epilogue warps have finished with the previous tile's: the input
+                // factor (GLU) or output factor (other modes), and for the GLU the
+                // inverse 2^-k of the power of two its f16 outputs are divided by
                 if (tc > 0 && !role_wait(smem_u32(rsempty), (tc - 1) & 1, abort_flag, lim, args.status, 9)) break;
-                for (int i = eth; i < nrows; i += NEPI * 32)
+                uint8_t *sas = reinterpret_cast<uint8_t *>(srs + BN);
+                for (int i = eth; i < nrows; i += NEPI * 32) {
                     srs[i] = args.rscale ? __ldg(args.rscale + row0 + i) : 1.f;
+                    if (MODE == OUT_GLU_F16)     // k of the output's divisor 2^k, one byte
+                        sas[i] = args.ascale ? (uint8_t)((__float_as_uint(__ldg(args.ascale + row0 + i)) >> 23) - 127) : 0;
+                }
                 mbar_arrive(smem_u32(rsfull));
                 if (!role_wait(smem_u32(rsfull), tc & 1, abort_flag, lim, args.status, 9)) break;
             }
@@ -477,8 +484,8 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 // before any of the chunk's global stores (through generic pointers the
                 // compiler cannot order a shared read above an earlier store); A8 reads them
                 // in its first pass, which stores nothing
-                float rsv[16];
-                if constexpr (MODE == OUT_GLU_F16 && KIND != EPI_A8) {
+                float rsv[16], asv[16];
+                if constexpr (MODE != OUT_GLU_F16 || KIND != EPI_A8) {
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const float4 f = reinterpret_cast<const float4 *>(srs + c * 16)[w];
@@ -487,6 +494,13 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         rsv[4 * w + 2] = f.z;
                         rsv[4 * w + 3] = f.w;
                     }
+                }
+                if constexpr (MODE == OUT_GLU_F16 && KIND != EPI_A8) {
+                    const uint4 e = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(srs + BN) + c * 16);
+                    const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)     // 2^-k
+                        asv[j] = __uint_as_float((127u - ((ew[j >> 2] >> (8 * (j & 3))) & 0xFFu)) << 23);
                 }
                 uint32_t v0[16], v1[16];
                 tmem_ld16(tbase + c * 16, v0);
@@ -547,16 +561,17 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                                         (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
                                 else
                                     a = fmaf(hv, tanh_approx(hv), hv) * uv;
+                                a *= asv[j];                // exact power of two keeping |a| inside f16
                                 bad |= !(fabsf(a) <= 65504.f);
                                 reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
                             } else if (MODE == OUT_BF16) {
                                 uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                                o[row] = f32_to_bf16(__uint_as_float(v0[j]) * fw0);
-                                if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * fw1);
+                                o[row] = f32_to_bf16(__uint_as_float(v0[j]) * (fw0 * rsv[j]));
+                                if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * (fw1 * rsv[j]));
                             } else {
                                 uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                                o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * fw0);
-                                if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * fw1);
+                                o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * (fw0 * rsv[j]));
+                                if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * (fw1 * rsv[j]));
                             }
                         }
                     }
@@ -566,7 +581,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(tempty + acc));
-                if (MODE == OUT_GLU_F16) mbar_arrive(smem_u32(rsempty));
+                mbar_arrive(smem_u32(rsempty));
             }
         }
         if (bad) set_status(args.status, K3MOE_ERR_RANGE, 2);

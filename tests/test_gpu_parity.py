@@ -104,6 +104,30 @@ def test_tensor_path_switch_boundaries(T):
     assert_parity(compare(cfg, g, ref))
 
 
+@pytest.mark.parametrize("path,name,T", [(TEN, "SMALL_ALIGNED", 40), (TEN, "SMALL_ALIGNED", 300),
+                                         (TEN, "SMALL_ALIGNED", 1500), (TEN, "SMALL_SHARED", 40),
+                                         (TEN, "SMALL_SHARED", 150), (GEN, "SMALL_ALIGNED", 40)],
+                         ids=["gemv", "tmem_a_192", "smem_a_256", "shared_n32", "shared_n256", "generic"])
+def test_glu_outputs_past_the_f16_range(path, name, T):
+    # x scaled by 2^9 (exact in BF16): the GLU outputs reach ~1e6-1e7, far past f16's
+    # 65504; every f16 GLU store divides its row by a power of two from the bound
+    # |a| <= |g| |u| <= ||w1_r|| ||w3_r|| ||h||^2, the down projection multiplies it back
+    cfg = getattr(synth, name).with_tokens(T)
+    dw = device_weights(cfg)
+    x = synth.f64_to_bf16_bits(synth.bf16_bits_to_f32(synth.gen_x(cfg)).astype(np.float64) * 512.0)
+    g = run_gpu(cfg, path, x=x, dw=dw)
+    assert g["status"] == 0 and g["path"] == path
+    ref = oracle_rows(cfg, dw.dense, x)
+    assert_parity(compare(cfg, g, ref))
+    # the oracle's GLU output of token 0's first expert is past the f16 range
+    res = oracle.forward(cfg, dw.dense, {int(e): synth.gen_expert(cfg, int(e)) for e in ref["idx"][0]}, x[:1],
+                         want_latent=True)
+    w1, w3, _ = [oracle.dequant(p, s) for p, s in synth.gen_expert(cfg, int(res["idx"][0, 0]))]
+    gv, uv = w1 @ res["h"][0], w3 @ res["h"][0]
+    with np.errstate(over="ignore"):
+        assert np.abs(gv / (1 + np.exp(-gv)) * uv).max() > 1e5
+
+
 def test_tensor_and_generic_paths_agree():
     cfg = synth.SMALL_SHARED.with_tokens(64)
     a = run_gpu(cfg, GEN)
