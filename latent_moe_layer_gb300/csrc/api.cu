@@ -330,8 +330,20 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->tiles = cv.take<int32_t>(4 * (R + c.n_experts + 1));
     ws->act = cv.take<float>(R * c.inter + 1);          // fp32 (generic) or f16 (tensor)
     ws->y = cv.take<float>(R * c.latent + 1);
-    // f16 expert inputs: the permuted h; with A8 also the MXFP8 GLU output [R, I]
-    ws->hperm = cv.take<uint16_t>(R * (c.latent > c.inter ? c.latent : c.inter) + 1);
+    // Tensor-path expert inputs in expert order: f16 h [R, L] (decode GEMV and tcgen05
+    // tiles), with A8 through the GEMV later the MXFP8-rounded GLU output [R, I] as f16;
+    // block-scaled A8 tiles: MXFP8 h [R, L] and GLU output [R, I], one byte each.  Before
+    // the weights are loaded the tensor path is assumed (the generic path does not use it).
+    {
+        const size_t LI = (size_t)(c.latent > c.inter ? c.latent : c.inter);
+        const bool gemv = R <= (size_t)c.n_experts * 24;
+        const bool tensor = h->loaded ? k3moe_path_for(h, T) == K3MOE_PATH_TENSOR : c.path != K3MOE_PATH_GENERIC;
+        size_t halves = 1;
+        if (tensor && c.a8 && gemv) halves = R * LI;
+        else if (tensor && c.a8) halves = (R * (size_t)(c.latent + c.inter) + 1) / 2;
+        else if (tensor) halves = R * (size_t)c.latent;
+        ws->hperm = cv.take<uint16_t>(halves + 1);
+    }
     ws->hscale = cv.take<float>(R + 1);
     ws->ascale = cv.take<float>(R + 1);
     ws->nrm = cv.take<uint16_t>(Tn * c.latent);
