@@ -69,7 +69,14 @@ size_t persistent_layout(const k3moe_config &c, uint8_t *base, k3moe_handle *h)
     int *flag = cv.take<int>(1);
     (void)flag;
     float *glu_bound = cv.take<float>(4);
+    // one counter per 128-row output tile of the decode-size dense GEMMs
+    const int cnt_up = (c.n_experts + 127) / 128 + (c.latent + 127) / 128;
+    const int cnt_n = cnt_up + (c.hidden + 127) / 128;
+    int *dcnt = cv.take<int>(cnt_n);
     if (h) {
+        h->d_dense_cnt = dcnt;
+        h->dense_cnt_up = cnt_up;
+        h->dense_cnt_n = cnt_n;
         h->d_status = st;
         for (int i = 0; i < 6; ++i) h->d_eptr[i] = tabs[i];
         h->d_shtab = shtab;
@@ -255,6 +262,7 @@ int k3moe_load_weights(k3moe_handle *h, const k3moe_weights *w, void *persistent
     h->persist_bytes = persistent_bytes;
     persistent_layout(c, h->persist, h);
     K3_CUDA_TRY(cudaMemsetAsync(h->d_status, 0, sizeof(int) * ST_COUNT, st));
+    K3_CUDA_TRY(cudaMemsetAsync(h->d_dense_cnt, 0, sizeof(int) * h->dense_cnt_n, st));
     for (int i = 0; i < 6; ++i)
         K3_CUDA_TRY(cudaMemcpyAsync((void *)h->d_eptr[i], tabs[i], sizeof(void *) * c.n_experts,
                                     cudaMemcpyHostToDevice, st));
@@ -511,6 +519,9 @@ int k3moe_status(k3moe_handle *h, cudaStream_t st)
     K3_CUDA_TRY(cudaStreamSynchronize(st));
     K3_CUDA_TRY(cudaMemcpy(v, h->d_status, sizeof(v), cudaMemcpyDeviceToHost));
     K3_CUDA_TRY(cudaMemsetAsync(h->d_status, 0, sizeof(int) * 2, st));
+    // a device-side failure may have stopped a dense GEMM between its tiles' arrivals:
+    // its split-K counters start from zero again
+    if (v[ST_CODE]) K3_CUDA_TRY(cudaMemsetAsync(h->d_dense_cnt, 0, sizeof(int) * h->dense_cnt_n, st));
     K3_CUDA_TRY(cudaStreamSynchronize(st));
     return v[ST_CODE];
 }

@@ -8,7 +8,8 @@
 // each with its own weight tensor map, K and output: the router (fp32 weights
 // held as BF16 hi + lo, contracted over K' = 2H against x read twice, which
 // keeps the logits fp32-accurate) and the down projection run together.
-// Split-K writes fp32 partials that k3_launch_dense_reduce sums in a fixed order.
+// Split-K writes fp32 partials that k3_launch_dense_reduce sums in a fixed order, or
+// (weight-stationary kernel) the last split of each tile to finish sums them.
 #include <cudaTypedefs.h>
 
 #include "dense_tc.h"
@@ -264,6 +265,20 @@ struct DenseWsSmem {
     static constexpr int BYTES = OFF_BAR + N_BAR * 8 + 16 + 1024;
 };
 
+// Named barrier 1 over the 8 epilogue warps (256 threads); the _and form returns
+// whether every thread passed a true predicate.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool epi_bar_and(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 256, q;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
 template <int TNS, int NS>
 __global__ void __launch_bounds__(DN_THREADS, 2) dense_ws_kernel(const __grid_constant__ CUtensorMap amap,
                                                                const __grid_constant__ CUtensorMap bmap0,
@@ -279,6 +294,7 @@ __global__ void __launch_bounds__(DN_THREADS, 2) dense_ws_kernel(const __grid_co
     uint64_t *tfull = empty + NS, *tempty = tfull + 2, *drain = tempty + 2;
     uint32_t *tmem_holder = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+    volatile int *last_flag = (volatile int *)(tmem_holder + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tn = min(TNS, max(16, (args.M + 15) & ~15));      // MMA N
     const int total = args.seg[0].n_tiles * args.seg[0].splits +
@@ -373,30 +389,83 @@ __global__ void __launch_bounds__(DN_THREADS, 2) dense_ws_kernel(const __grid_co
         const int q = warp & 3;                       // TMEM lanes 32q .. 32q + 31 = weight rows
         const int half = (warp - 2) >> 2;             // token chunks c with c % 2 == half
         uint32_t tc = 0;
-        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++tc) {
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const DnTile d = dn_tile(args, t, 1, DN_BM);
             const DenseSeg S = dn_seg(args, d.seg);
             const int acc = (int)(tc & 1);
             const int n = d.n0 + 32 * q + lane;          // output column (weight row)
-            if (!dn_wait(smem_u32(tfull + acc), (tc >> 1) & 1, abort_flag, args.status, 28)) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * TNS;
-            for (int c = half; c < tn / 16; c += 2) {
-                uint32_t v[16];
-                tmem_ld16(tbase + c * 16, v);
-                tc_wait_ld();
-                if (n < S.n_out) {
-                    float *o = reinterpret_cast<float *>(S.out) + ((size_t)d.split * args.M) * S.ldo + S.col0 + n;
+            const bool ok = !*abort_flag && dn_wait(smem_u32(tfull + acc), (tc >> 1) & 1, abort_flag, args.status, 28);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * TNS;
+                for (int c = half; c < tn / 16; c += 2) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c * 16, v);
+                    tc_wait_ld();
+                    if (n < S.n_out) {
+                        float *o = reinterpret_cast<float *>(S.out) + ((size_t)d.split * args.M) * S.ldo + S.col0 + n;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = 16 * c + j;               // token
-                        if (m < args.M) o[(size_t)m * S.ldo] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * c + j;               // token
+                            if (m < args.M) o[(size_t)m * S.ldo] = __uint_as_float(v[j]);
+                        }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(tempty + acc));
+            if (!args.tile_cnt) {
+                if (!ok) break;
+                continue;
+            }
+            // The tile's last split to arrive sums the partials of all splits in split order
+            // (the fixed order of the separate reduction).  The 256 epilogue threads agree on
+            // continuing before any of them waits at the named barrier again.
+            __threadfence();
+            if (!epi_bar_and(ok)) break;
+            const int id = (d.seg ? args.seg[0].n_tiles : 0) + d.n0 / DN_BM;
+            if (warp == 2 && lane == 0) *last_flag = atomicAdd(args.tile_cnt + id, 1) == S.splits - 1;
+            epi_bar();
+            if (*last_flag) {
+                // thread i: columns d.n0 + 4 (i % 32) .. +3 of token rows i / 32 + 8 j; every
+                // split's 16-byte partial is loaded before the sum in split order
+                __threadfence();
+                const int i = threadIdx.x - 64;              // 0 .. 255
+                const int col = d.n0 + 4 * (i & 31);
+                if (col < S.n_out) {
+                    const float *p = reinterpret_cast<const float *>(S.out) + S.col0 + col;
+                    for (int m = i >> 5; m < args.M; m += 8) {
+                        float r[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int s0 = 0; s0 < S.splits; s0 += 8) {     // 8 splits' loads in flight
+                            float4 v[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (s0 + j < S.splits)
+                                    v[j] = __ldcg(reinterpret_cast<const float4 *>(
+                                        p + ((size_t)(s0 + j) * args.M + m) * S.ldo));
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (s0 + j < S.splits) {
+                                    r[0] += v[j].x;
+                                    r[1] += v[j].y;
+                                    r[2] += v[j].z;
+                                    r[3] += v[j].w;
+                                }
+                        }
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            if (col + q2 >= S.n_out) break;
+                            const size_t o = (size_t)m * S.red_ldo + col + q2;
+                            if (S.red_mode == DN_OUT_BF16)
+                                reinterpret_cast<uint16_t *>(S.red_out)[o] = f32_to_bf16(r[q2]);
+                            else
+                                reinterpret_cast<float *>(S.red_out)[o] = r[q2];
+                        }
+                    }
+                }
+                if (i == 0) args.tile_cnt[id] = 0;
+            }
         }
     }
     tc_fence_before();

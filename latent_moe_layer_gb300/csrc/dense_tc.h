@@ -19,6 +19,11 @@ struct DenseSeg {
     void *out;
     int ldo;
     int col0;
+    // weight-stationary kernel with DenseArgs::tile_cnt: where the last split of a tile
+    // writes the tile's sum over splits (red_mode DN_OUT_F32 or DN_OUT_BF16, [m * red_ldo + n])
+    void *red_out;
+    int red_mode;
+    int red_ldo;
 };
 
 struct DenseArgs {
@@ -26,6 +31,9 @@ struct DenseArgs {
     int nseg;
     int M;           // token rows
     int *status;
+    // weight-stationary kernel: one arrival counter per output tile (segment 0's tiles
+    // first), zero before the launch and left zero by it; nullptr = partials only
+    int *tile_cnt;
 };
 
 }  // namespace k3
@@ -33,7 +41,9 @@ struct DenseArgs {
 // X rows [rows, cols] BF16 (or weights): box 64 x box_rows, 128-byte swizzle.
 bool k3_encode_bf16_rows(CUtensorMap *m, const void *base, int rows, int cols, int box_rows);
 // Decode sizes (T <= 256): the weight-stationary kernel (MMA M = 128 weight rows, N =
-// tokens), split-K fp32 partials only.  a: x rows [T, K] with box rows k3_dense_ws_rows(T).
+// tokens), split-K fp32 partials; with args.tile_cnt the last split of each tile to
+// finish also sums the tile's partials in split order into red_out.  a: x rows [T, K]
+// with box rows k3_dense_ws_rows(T).
 int k3_dense_ws_rows(int T);
 int k3_launch_dense_ws(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const k3::DenseArgs &args,
                        int num_sms, cudaStream_t st);

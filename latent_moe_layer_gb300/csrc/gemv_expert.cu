@@ -16,7 +16,8 @@
 // {8c+4, 8c+5 | 8c+6, 8c+7}; the B fragments read the activations at the same
 // K.  The MMAs run on the plain E2M1 values (exact in f16) and the block's fp32
 // partial sum is multiplied by 2^(e - 127) (exact in fp32; code 0 is taken as 0)
-// and added to the row's accumulator.
+// and added to the row's accumulator (packed fp32x2 FMAs: the two token columns a
+// thread holds for one row share the row's scale).
 #include "gemv_expert.h"
 #include "tc_expert.cuh"
 
@@ -47,6 +48,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+
+// {d0, d1} += {a0, a1} * s: two fp32 FMAs, each rounded once (as fmaf), in one packed instruction.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float s)
+{
+    asm("{\n\t.reg .b64 d, a, s;\n\tmov.b64 d, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+        "fma.rn.f32x2 d, a, s, d;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(s));
 }
 
 // Token row of B (within an 8-token block) that MMA column n reads: 0, 4, 1, 5, 2, 6, 3, 7.
@@ -155,10 +165,8 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                         float p[4] = {0.f, 0.f, 0.f, 0.f};
                         mma16816(p, a0, hb[nb].x, hb[nb].y);
                         mma16816(p, a1, hb[nb].z, hb[nb].w);
-                        acc[m][nb][0] = fmaf(p[0], fa, acc[m][nb][0]);
-                        acc[m][nb][1] = fmaf(p[1], fa, acc[m][nb][1]);
-                        acc[m][nb][2] = fmaf(p[2], fb, acc[m][nb][2]);
-                        acc[m][nb][3] = fmaf(p[3], fb, acc[m][nb][3]);
+                        ffma2(acc[m][nb][0], acc[m][nb][1], p[0], p[1], fa);
+                        ffma2(acc[m][nb][2], acc[m][nb][3], p[2], p[3], fb);
                     }
                 }
             }

@@ -209,6 +209,10 @@ struct k3moe_handle {
     uint8_t *d_rowmax = nullptr;               // tensor-path per-row max exponent bytes
     uint16_t *d_router_hilo = nullptr;         // tensor-path router weights as BF16 [E, 2H] (hi | lo)
     float *d_glu_bound = nullptr;              // largest gate / up row L2 norms: routed w1, w3, shared ws1, ws3
+    int *d_dense_cnt = nullptr;                // split-K arrival counters of the weight-stationary dense
+                                               // GEMMs: router + down_proj tiles, then up_proj tiles
+    int dense_cnt_up = 0;                      // first up_proj counter
+    int dense_cnt_n = 0;                       // counters in all
     size_t tmap_count = 0;
     k3_prof *prof = nullptr;                   // stage timing, when enabled
     // split-K plans of the decode-size dense GEMMs per token count (0 = not planned yet):

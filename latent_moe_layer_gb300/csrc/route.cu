@@ -11,84 +11,79 @@
 
 namespace k3 {
 
-// Top-K of one token, one warp.  Lane l owns keys j = l + 32 i (a column of a
-// [MAXP][32] tile in shared memory) and keeps the best untaken key of its
-// column.  Each of the K rounds takes the warp-wide maximum of the lane bests
-// (equal keys: lower index), marks it taken, and the warp rescans only the
-// winning lane's column.  NaN keys rank below every number.  Writes idx in
-// selection order (and to sidx when given) and the weights
+// Order-preserving image of a key in uint32: a larger float gives a larger integer
+// (-0 is first turned into +0, so that equal keys stay equal).  Every key, -inf
+// included, maps to at least 0x007FFFFF; 0 marks "no key".
+__device__ __forceinline__ uint32_t key_bits(float k)
+{
+    if (k == 0.f) k = 0.f;
+    const uint32_t u = __float_as_uint(k);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-K of one token, one warp.  Lane l owns keys j = l + 32 i (row l of a
+// [32][MAXP + 1] tile of key images in shared memory) and keeps the best untaken
+// key of its row.  Each of the K rounds takes the warp-wide maximum of the lane
+// bests (equal keys: lower index) with two warp reductions (max of the key, then
+// min of the index among the lanes holding it), marks it taken, and the warp
+// rescans only the winning lane's row the same way.  NaN keys rank below every
+// number.  Writes idx in selection order (and to sidx when given) and the weights
 // sigmoid(l_k) / sum_sel sigmoid(l) * scaling.
 template <int MAXP>
 __device__ __forceinline__ void topk_warp(const float *__restrict__ lrow, const float *__restrict__ bias, int E,
-                                          int K, float scaling, float (*col)[32], int lane,
+                                          int K, float scaling, uint32_t (*row)[MAXP + 1], int lane,
                                           int32_t *__restrict__ idx_row, float *__restrict__ w_row, int *sidx)
 {
-    float bk = -INFINITY;
-    int bj = 0x7fffffff;
+    constexpr uint32_t ALL = 0xffffffffu, NONE = 0xffffffffu;
+    uint32_t bk = 0, bj = NONE;
 #pragma unroll
     for (int i = 0; i < MAXP; ++i) {
         const int j = lane + 32 * i;
-        float k = -INFINITY;
+        uint32_t u = 0;
         if (j < E) {
             const float l = lrow[j];
-            k = bias ? 1.0f / (1.0f + expf(-l)) + bias[j] : l;
+            float k = bias ? 1.0f / (1.0f + expf(-l)) + bias[j] : l;
             if (k != k) k = -INFINITY;
-            if (k > bk || bj == 0x7fffffff) {     // first valid key, then strictly larger
-                bk = k;
+            u = key_bits(k);
+            if (u > bk) {                        // strictly larger: the lower index keeps equal keys
+                bk = u;
                 bj = j;
             }
         }
-        col[i][lane] = k;
+        row[lane][i] = u;
     }
     __syncwarp();
     uint32_t taken = 0;          // bit i: key lane + 32 i taken (owner lane's view)
     int sel_j = 0;
     for (int s = 0; s < K; ++s) {
-        float wk = bk;
-        int wj = bj;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, wk, off);
-            const int oj = __shfl_xor_sync(0xffffffffu, wj, off);
-            if (ok > wk || (ok == wk && oj < wj)) {
-                wk = ok;
-                wj = oj;
-            }
-        }
+        const uint32_t wk = __reduce_max_sync(ALL, bk);
+        const uint32_t wj = __reduce_min_sync(ALL, bk == wk ? bj : NONE);
         const int owner = wj & 31;
         if (lane == owner) taken |= 1u << (wj >> 5);
-        const uint32_t otaken = __shfl_sync(0xffffffffu, taken, owner);
-        // rescan the owner's column: lane i looks at key owner + 32 i
-        float ck = -INFINITY;
-        int cj = 0x7fffffff;
+        const uint32_t otaken = __shfl_sync(ALL, taken, owner);
+        // rescan the owner's row: lane i looks at key owner + 32 i
+        uint32_t ck = 0, cj = NONE;
         if (lane < MAXP) {
             const int j = owner + 32 * lane;
             if (j < E && !((otaken >> lane) & 1u)) {
-                ck = col[lane][owner];
+                ck = row[owner][lane];
                 cj = j;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, ck, off);
-            const int oj = __shfl_xor_sync(0xffffffffu, cj, off);
-            if (ok > ck || (ok == ck && oj < cj)) {
-                ck = ok;
-                cj = oj;
-            }
-        }
+        const uint32_t nk = __reduce_max_sync(ALL, ck);
+        const uint32_t nj = __reduce_min_sync(ALL, ck == nk ? cj : NONE);
         if (lane == owner) {
-            bk = ck;
-            bj = cj;
+            bk = nk;
+            bj = nj;
         }
-        if (lane == s) sel_j = wj;
+        if (lane == s) sel_j = (int)wj;
     }
     // weights: sigma(l) of the selected experts over their sum (a butterfly sum: every
     // lane adds the same operand pairs, so all lanes hold the same total)
     const float sg = lane < K ? 1.0f / (1.0f + expf(-lrow[sel_j])) : 0.f;
     float ssum = sg;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
+    for (int off = 16; off > 0; off >>= 1) ssum += __shfl_xor_sync(ALL, ssum, off);
     if (lane < K) {
         idx_row[lane] = sel_j;
         w_row[lane] = sg / ssum * scaling;
@@ -107,7 +102,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     // the permutation's expert histogram starts from zero (the next kernel counts into it)
     if (counts_zero && blockIdx.x == 0)
         for (int i = threadIdx.x; i < E; i += blockDim.x) counts_zero[i] = 0;
-    __shared__ float skey[8][MAXP][32];
+    __shared__ uint32_t skey[8][32][MAXP + 1];
     const int wl = threadIdx.x >> 5;
     const int warp = blockIdx.x * 8 + wl;
     const int lane = threadIdx.x & 31;
@@ -131,41 +126,57 @@ __global__ void perm_count_kernel(const int32_t *__restrict__ idx, int n, int E,
     atomicAdd(counts + e, 1);
 }
 
+// Inclusive scan over a warp (shuffles).
+__device__ __forceinline__ int warp_scan_incl(int v, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
+    }
+    return v;
+}
+
 // One CTA of 1024 threads: offsets = exclusive scan of counts; active-expert
 // list; tile list for the tensor path (expert, first row, rows) with at most
 // tile_n rows each.  Ends with the CTA synchronised and its writes visible to it.
+// Each 1024-expert chunk is scanned per warp, then over the 32 warp totals.
 __device__ __forceinline__ void perm_scan_block(const int32_t *counts, int E, int tile_n,
                                                 int32_t *__restrict__ offsets, int32_t *__restrict__ active,
                                                 int4 *__restrict__ tiles, int32_t *__restrict__ meta)
 {
-    __shared__ int s_cnt[1024], s_act[1024], s_til[1024];
+    __shared__ int s_w[3][32];
     __shared__ int base_rows, base_act, base_til;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) base_rows = base_act = base_til = 0;
     __syncthreads();
     for (int e0 = 0; e0 < E; e0 += 1024) {
-        int e = e0 + tid;
-        int c = e < E ? counts[e] : 0;
-        int nt = (tile_n > 0) ? (c + tile_n - 1) / tile_n : 0;
-        s_cnt[tid] = c;
-        s_act[tid] = c > 0;
-        s_til[tid] = nt;
+        const int e = e0 + tid;
+        const int c = e < E ? counts[e] : 0;
+        const int nt = (tile_n > 0) ? (c + tile_n - 1) / tile_n : 0;
+        int sc = warp_scan_incl(c, lane), sa = warp_scan_incl(c > 0, lane), st = warp_scan_incl(nt, lane);
+        if (lane == 31) {
+            s_w[0][w] = sc;
+            s_w[1][w] = sa;
+            s_w[2][w] = st;
+        }
         __syncthreads();
-        for (int off = 1; off < 1024; off <<= 1) {     // inclusive Hillis-Steele scans
-            int a = tid >= off ? s_cnt[tid - off] : 0;
-            int b = tid >= off ? s_act[tid - off] : 0;
-            int d = tid >= off ? s_til[tid - off] : 0;
-            __syncthreads();
-            s_cnt[tid] += a;
-            s_act[tid] += b;
-            s_til[tid] += d;
-            __syncthreads();
+        if (w == 0) {
+            s_w[0][lane] = warp_scan_incl(s_w[0][lane], lane);
+            s_w[1][lane] = warp_scan_incl(s_w[1][lane], lane);
+            s_w[2][lane] = warp_scan_incl(s_w[2][lane], lane);
+        }
+        __syncthreads();
+        if (w > 0) {
+            sc += s_w[0][w - 1];
+            sa += s_w[1][w - 1];
+            st += s_w[2][w - 1];
         }
         if (e < E) {
-            int row0 = base_rows + s_cnt[tid] - c;
+            int row0 = base_rows + sc - c;
             offsets[e] = row0;
-            if (c > 0) active[base_act + s_act[tid] - 1] = e;
-            int t0 = base_til + s_til[tid] - nt;
+            if (c > 0) active[base_act + sa - 1] = e;
+            int t0 = base_til + st - nt;
             for (int q = 0; q < nt; ++q) {
                 int r = q * tile_n;
                 tiles[t0 + q] = make_int4(e, row0 + r, min(tile_n, c - r), 0);
@@ -173,9 +184,9 @@ __device__ __forceinline__ void perm_scan_block(const int32_t *counts, int E, in
         }
         __syncthreads();
         if (tid == 1023) {
-            base_rows += s_cnt[1023];
-            base_act += s_act[1023];
-            base_til += s_til[1023];
+            base_rows += sc;
+            base_act += sa;
+            base_til += st;
         }
         __syncthreads();
     }
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     int32_t *__restrict__ tok_of, int32_t *__restrict__ row_of, int *status)
 {
     griddep_enter();
-    extern __shared__ float rs_keys[];                // [32][MAXP][32]
+    extern __shared__ uint32_t rs_keys[];             // [32 warps][32][MAXP + 1]
     __shared__ int s_idx[1024], s_hist[1024];
     __shared__ uint32_t s_tok[1024];                 // bit t: token t selected expert e (T <= 32)
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, n = T * K;
@@ -219,8 +230,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     __syncthreads();
     if (w < T)
         topk_warp<MAXP>(logits + (size_t)w * E, bias, E, K, scaling,
-                        reinterpret_cast<float(*)[32]>(rs_keys + (size_t)w * MAXP * 32), lane, idx + (size_t)w * K,
-                        wts + (size_t)w * K, s_idx + w * K);
+                        reinterpret_cast<uint32_t(*)[MAXP + 1]>(rs_keys + (size_t)w * 32 * (MAXP + 1)), lane,
+                        idx + (size_t)w * K, wts + (size_t)w * K, s_idx + w * K);
     __syncthreads();
     if (tid < n) {
         const int e = s_idx[tid];
@@ -401,7 +412,7 @@ static int launch_route_small(const k3moe_handle *h, const k3_ws &ws, int T, int
 {
     const k3moe_config &c = h->cfg;
     auto kern = route_small_kernel<MAXP>;
-    const size_t smem = sizeof(float) * 32 * MAXP * 32;
+    const size_t smem = sizeof(uint32_t) * 32 * 32 * (MAXP + 1);
     static unsigned long long attr_set = 0;
     if (!k3_smem_attr(kern, (int)smem, attr_set)) return K3MOE_ERR_CUDA;
     const float *bias = c.has_select_bias ? h->bias : nullptr;

@@ -347,8 +347,9 @@ int k3_tc_prepare(k3moe_handle *h, const uint8_t *const *const tabs[6], cudaStre
 // differing by at most one K step) round-robin over `grid_max` CTAs.  Costs are
 // in K steps (16 KB of weights): a unit costs its K steps plus its fp32 partial
 // tile (rows x 128 x 4 bytes = rows / 32 K steps), and the reduction reads every
-// partial once, spread over the whole GPU.  The plan minimises the busiest CTA's
-// load plus the reduction; ties go to fewer units.
+// partial once (counted as spread over the whole GPU; in the weight-stationary
+// kernel the last split of each tile reads its tile's partials).  The plan
+// minimises the busiest CTA's load plus the reduction; ties go to fewer units.
 static void plan_splits(DenseSeg *seg, int nseg, int T, int grid_max, bool ws)
 {
     const int mt = ws ? 1 : (T + 127) / 128;
@@ -452,6 +453,16 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
         r.ldo = d.ldo = Ep + L;
         r.col0 = 0;
         d.col0 = Ep;
+        if (ws_k) {
+            // the last split of each tile writes the logits (fp32) and h (BF16) itself
+            a.tile_cnt = h->d_dense_cnt;
+            r.red_out = ws.logits;
+            r.red_mode = DN_OUT_F32;
+            r.red_ldo = E;
+            d.red_out = ws.h;
+            d.red_mode = DN_OUT_BF16;
+            d.red_ldo = L;
+        }
     } else {
         r.splits = d.splits = 1;
         r.mode = DN_OUT_F32;
@@ -470,7 +481,7 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
                        : k3_launch_dense_tc(small ? 128 : 256, ax, br, bd, a, h->num_sms, st)))
             return rc;
     }
-    if (small) {
+    if (small && !ws_k) {
         k3_stage sg(h, K3MOE_STAGE_DOWN, st);
         if ((rc = k3_launch_dense_reduce(ws.part, r.splits, T, Ep + L, 0, E, ws.logits, nullptr, E, st))) return rc;
         if ((rc = k3_launch_dense_reduce(ws.part, d.splits, T, Ep + L, Ep, L, nullptr, ws.h, L, st))) return rc;
@@ -506,9 +517,16 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.splits = 1;
     if (small) dense_splits(h, a.seg, 1, T, 2, dense_ws(T));
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
+    if (ws_k) {
+        // the last split of each tile writes the output itself
+        a.tile_cnt = h->d_dense_cnt + h->dense_cnt_up;
+        u.red_out = out16 ? (void *)out16 : (void *)ws.o32;
+        u.red_mode = out16 ? DN_OUT_BF16 : DN_OUT_F32;
+        u.red_ldo = H;
+    }
     int rc = ws_k ? k3_launch_dense_ws(an, bu, bu, a, h->num_sms, st) : k3_launch_dense_tc(bn, an, bu, bu, a, h->num_sms, st);
     if (rc) return rc;
-    if (small)
+    if (small && !ws_k)
         rc = k3_launch_dense_reduce(ws.part, u.splits, T, H, 0, H, out16 ? nullptr : ws.o32, out16, H, st);
     return rc;
 }
