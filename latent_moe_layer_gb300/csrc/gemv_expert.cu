@@ -175,7 +175,9 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
     return true;
 }
 
-template <int NMAT, int NS, int MODE>
+// MAXNB = 2: the K loop exists for 8- and 16-token tiles.  MAXNB = 1: for 8 only (tiles of
+// at most 8 tokens), which leaves the compiler more registers for the one loop.
+template <int NMAT, int NS, int MODE, int MAXNB>
 __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_constant__ CUtensorMap bmap,
                                                              const GemvArgs a)
 {
@@ -257,14 +259,14 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) acc[m][h][q] = 0.f;
-            const bool ok = nt > 8 ? gemv_k_loop<NMAT, NS, 2>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
+            const bool ok = (MAXNB == 2 && nt > 8) ? gemv_k_loop<NMAT, NS, 2>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
                                                               sa, kb, it, acc)
                                    : gemv_k_loop<NMAT, NS, 1>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
                                                               sa, kb, it, acc);
             if (!ok) break;
             // epilogue: acc[m][nb][0..1] = (row ra, tokens 8 nb + 2c, +1); [2..3] = (row rb, same tokens)
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb)
+            for (int nb = 0; nb < MAXNB; ++nb)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int tok = 8 * nb + tok_perm(2 * c + (q & 1));
@@ -298,12 +300,12 @@ __global__ void __launch_bounds__(288, 2) gemv_expert_kernel(const __grid_consta
 
 using namespace k3;
 
-template <int NMAT, int NS, int MODE>
+template <int NMAT, int NS, int MODE, int MAXNB>
 static int launch_gemv(const CUtensorMap &bmap, const GemvArgs &args, int max_items, int num_sms, cudaStream_t st)
 {
     using SM = GvSmem<NMAT, NS>;
     static_assert(2 * SM::BYTES <= 228 * 1024, "two CTAs per SM");
-    auto kern = gemv_expert_kernel<NMAT, NS, MODE>;
+    auto kern = gemv_expert_kernel<NMAT, NS, MODE, MAXNB>;
     static unsigned long long attr_set = 0;
     if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int grid = max(1, min(max_items, 2 * num_sms));
@@ -312,10 +314,15 @@ static int launch_gemv(const CUtensorMap &bmap, const GemvArgs &args, int max_it
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
 
-int k3_launch_gemv_expert(int glu, int mode, const CUtensorMap &bmap, const GemvArgs &args, int max_items,
-                          int num_sms, cudaStream_t st)
+int k3_launch_gemv_expert(int glu, int mode, int max_nb, const CUtensorMap &bmap, const GemvArgs &args,
+                          int max_items, int num_sms, cudaStream_t st)
 {
-    if (glu) return launch_gemv<2, 2, GV_GLU_F16>(bmap, args, max_items, num_sms, st);
-    if (mode == GV_BF16) return launch_gemv<1, 4, GV_BF16>(bmap, args, max_items, num_sms, st);
+    if (max_nb == 1) {
+        if (glu) return launch_gemv<2, 2, GV_GLU_F16, 1>(bmap, args, max_items, num_sms, st);
+        if (mode == GV_BF16) return launch_gemv<1, 4, GV_BF16, 1>(bmap, args, max_items, num_sms, st);
+    } else {
+        if (glu) return launch_gemv<2, 2, GV_GLU_F16, 2>(bmap, args, max_items, num_sms, st);
+        if (mode == GV_BF16) return launch_gemv<1, 4, GV_BF16, 2>(bmap, args, max_items, num_sms, st);
+    }
     return K3MOE_ERR_UNSUPPORTED;
 }

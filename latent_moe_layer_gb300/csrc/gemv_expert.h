@@ -27,6 +27,7 @@ struct GemvArgs {
 
 }  // namespace k3
 
-// bmap: f16 activation rows [R, K], box 64 x 16, 128-byte swizzle.
-int k3_launch_gemv_expert(int glu, int mode, const CUtensorMap &bmap, const k3::GemvArgs &args, int max_items,
-                          int num_sms, cudaStream_t st);
+// bmap: f16 activation rows [R, K], box 64 x 16, 128-byte swizzle.  max_nb: 2 for tiles of up
+// to 16 tokens; 1 for tiles of at most 8 (a kernel with fewer live registers).
+int k3_launch_gemv_expert(int glu, int mode, int max_nb, const CUtensorMap &bmap, const k3::GemvArgs &args,
+                          int max_items, int num_sms, cudaStream_t st);

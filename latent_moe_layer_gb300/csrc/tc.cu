@@ -654,6 +654,10 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     const int L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
     const int R = T * K;
     const bool gemv = pick_bn(T, K, E) == 32;   // routed experts at decode sizes: the streaming GEMV
+    // With at most two tokens per expert on average the GEMV takes tiles of at most 8 tokens
+    // (an expert with more gets several tiles, each streaming its weights): its kernel for
+    // 8-token tiles keeps more registers for the one K loop and runs faster.
+    const int gv_nb = (size_t)T * K <= 2 * (size_t)E ? 1 : 2;
     const bool mx = c.a8 && !gemv;              // A8 at tile sizes: block-scaled MXFP4 x MXFP8 MMAs
     const int bn = mx ? MX_BN : pick_bn(T, K, E);
     int rc;
@@ -663,8 +667,8 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     if (c.a8 && gemv && (rc = k3_launch_mx8_rows(ws.h, 0, ws.h, 0, (size_t)T * L, h->d_status, h->num_sms, st)))
         return rc;
     // top-K and the permutation; token tiles: <= 16 rows for the decode GEMV, bn for the tcgen05 GEMMs
-    if ((rc = k3_launch_route(h, ws, T, gemv ? 16 : bn, st))) return rc;
-    const int max_ntiles = (R + 15) / 16 + (E < R ? E : R);
+    if ((rc = k3_launch_route(h, ws, T, gemv ? 8 * gv_nb : bn, st))) return rc;
+    const int max_ntiles = (R + 7) / 8 + (E < R ? E : R);     // tiles of 8 rows or more
     if (mx) {
         // h as MXFP8 in expert order [R, L] (+ scales), the GLU output as MXFP8 [R, I] (+ scales)
         uint8_t *hq8 = (uint8_t *)ws.hperm, *aq8 = hq8 + (size_t)R * L;
@@ -785,7 +789,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
             k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
             CUtensorMap gb1;
             if (!encode_act(&gb1, ws.hperm, R, L, 16)) return K3MOE_ERR_CUDA;
-            if ((rc = k3_launch_gemv_expert(1, GV_GLU_F16, gb1, g1, max_ntiles * (I / 128), h->num_sms, st)))
+            if ((rc = k3_launch_gemv_expert(1, GV_GLU_F16, gv_nb, gb1, g1, max_ntiles * (I / 128), h->num_sms, st)))
                 return rc;
             // A8: the GLU output (fp32) rounded to MXFP8, as the down projection's f16 input
             if (c.a8 && (rc = k3_launch_mx8_rows(ws.act, 1, ws.hperm, 2, (size_t)R * I, h->d_status, h->num_sms,
@@ -796,7 +800,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
             k3_stage sg(h, K3MOE_STAGE_EXPERT_DOWN, st);
             CUtensorMap gb2;
             if (!encode_act(&gb2, act16, R, I, 16)) return K3MOE_ERR_CUDA;
-            if ((rc = k3_launch_gemv_expert(0, GV_BF16, gb2, g2, max_ntiles * (L / 128), h->num_sms, st)))
+            if ((rc = k3_launch_gemv_expert(0, GV_BF16, gv_nb, gb2, g2, max_ntiles * (L / 128), h->num_sms, st)))
                 return rc;
         }
     } else if ((rc = expert_pair(h, bn, bm1, bm2, a1, a2, max_ntiles * (I / EX_BM), max_ntiles * (L / EX_BM),

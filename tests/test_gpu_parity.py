@@ -91,16 +91,35 @@ def test_wide_scale_exponents(path, T):
 
 
 # Token counts on each side of the tensor path's internal switches (SMALL_ALIGNED:
-# E = 24, K = 4): the weight-stationary dense GEMMs up to T = 64, decode GEMV vs
-# tcgen05 tiles at T K = 24 E (T = 144), split-K dense GEMMs up to T = 256, the
-# chunked permutation from T = 512, 192-row tiles with the decoded weights in
-# TMEM vs 256-row tiles at T K = 192 E (T = 1152).
-@pytest.mark.parametrize("T", [1, 16, 17, 64, 65, 144, 145, 256, 257, 511, 512, 1152, 1153, 2000])
+# E = 24, K = 4): 8-token decode GEMV tiles up to T K = 2 E (T = 12), the weight-stationary
+# dense GEMMs up to T = 64, decode GEMV vs tcgen05 tiles at T K = 24 E (T = 144),
+# split-K dense GEMMs up to T = 256, the chunked permutation from T = 512, 192-row
+# tiles with the decoded weights in TMEM vs 256-row tiles at T K = 192 E (T = 1152).
+@pytest.mark.parametrize("T", [1, 12, 13, 16, 17, 64, 65, 144, 145, 256, 257, 511, 512, 1152, 1153, 2000])
 def test_tensor_path_switch_boundaries(T):
     cfg = synth.SMALL_ALIGNED.with_tokens(T)
     g = run_gpu(cfg, TEN)
     assert g["status"] == 0 and g["path"] == TEN
     ref = oracle_rows(cfg, device_weights(cfg).dense, g["x"])
+    assert_parity(compare(cfg, g, ref))
+
+
+@pytest.mark.parametrize("T", [12, 13], ids=["two_passes", "loop_16"])
+def test_gemv_tiles_past_8_tokens(T):
+    """A selection bias sends every token to the same 4 experts, so each touched expert
+    holds T > 8 rows.  At T K <= 2 E (T = 12) the decode GEMV takes tiles of at most 8
+    tokens, so each of those experts gets two tiles (8 + 4 rows) and its weights are
+    streamed twice; at T = 13 one 16-token tile per expert runs the 16-token K loop."""
+    base = synth.SMALL_ALIGNED.with_tokens(T)
+    cfg = synth.LayerConfig(**{**base.__dict__, "select_bias": True, "name": f"small_concentrated_t{T}"})
+    dense = synth.gen_dense(base)
+    dense.select_bias = np.zeros(cfg.E, np.float32)
+    dense.select_bias[[3, 7, 11, 19]] = 4.0
+    dw = k3moe.DeviceWeights(cfg, dense=dense)
+    g = run_gpu(cfg, TEN, dw=dw)
+    assert g["status"] == 0 and g["path"] == TEN
+    assert np.all(np.sort(g["idx"], axis=1) == [3, 7, 11, 19])
+    ref = oracle_rows(cfg, dense, g["x"])
     assert_parity(compare(cfg, g, ref))
 
 
