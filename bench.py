@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from one ncu capture of a 128-expert case at the K3 shapes, scaled by the
 # touched experts.  They hold for the kernel source whose sha256 prefix is
 # given; any other source reports traffic null until it is captured again.
-NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "e14d6195b013b711",
-               "per_expert": {("gate_up", "gemv"): 12.01e6, ("expert_down", "gemv"): 5.867e6}}
+NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "82a33b403f79e728",
+               "per_expert": {("gate_up", "gemv"): 12.00e6, ("expert_down", "gemv"): 5.866e6}}
 EXTRA_WORKLOADS = [2, 3, 4, "moderate", "3a8"]
 
 
