@@ -34,12 +34,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode expert-weight GB/s vs HBM peak; prefill TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per touched expert per launch of the decode GEMV,
-# from one ncu capture of a 128-expert case at the K3 shapes, scaled by the
-# touched experts.  They hold for the kernel source whose sha256 prefix is
-# given; any other source reports traffic null until it is captured again.
-NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "82a33b403f79e728",
-               "per_expert": {("gate_up", "gemv"): 12.00e6, ("expert_down", "gemv"): 5.866e6}}
+# DRAM bytes (read + write) per touched expert per launch of the decode GEMVs, from
+# ncu captures of 128-expert cases at the K3 shapes, scaled by the touched experts:
+# the fused gate/up + down launch at T=16 (8-token tiles), the separate 16-token-tile
+# launches at T=37 (4.6 rows per expert, as at T=256 with 896 experts).  They hold for
+# the kernel source whose sha256 prefix is given; any other source reports traffic
+# null until it is captured again.
+NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "3d9e64c1e7225346",
+               "per_expert": {("gate_up+expert_down", "gemv"): 18.37e6, ("gate_up", "gemv"): 12.24e6,
+                              ("expert_down", "gemv"): 5.883e6}}
 EXTRA_WORKLOADS = [2, 3, 4, "moderate", "3a8"]
 
 
@@ -357,6 +360,10 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
 
     # roofline of the dominant stage
     work = stage_work(cfg, touched, path_tensor)
+    # the decode GEMVs of both projections can run as one launch, timed as the gate/up stage
+    fused = stage_ms.get("gate_up", 0) > 0 and stage_ms.get("expert_down", 0) == 0
+    if fused:
+        work["gate_up"] = tuple(u + v for u, v in zip(work["gate_up"], work["expert_down"]))
     dom = max(stage_ms, key=lambda s: stage_ms[s])
     per_launch_ms = stage_ms[dom] / max(1, nfw)
     b, f = work[dom]
@@ -377,12 +384,14 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "traffic": None, "peak_kind": "bf16 dense, sustained"}
-    key = (dom, "gemv" if (path_tensor and cfg.T * cfg.K <= cfg.E * 24) else "other")
+    key = ("gate_up+expert_down" if fused and dom == "gate_up" else dom,
+           "gemv" if (path_tensor and cfg.T * cfg.K <= cfg.E * 24) else "other")
     traffic = ncu_traffic_per_expert()
     if key in traffic:
         roof["traffic"] = round(traffic[key] * touched)
         roof["traffic_source"] = "ncu dram bytes per touched expert x touched experts"
-    roof.update({"kernel_stage": dom, "per_launch_ms": round(per_launch_ms, 4),
+    roof.update({"kernel_stage": dom + ("+expert_down (one launch)" if fused and dom == "gate_up" else ""),
+                 "per_launch_ms": round(per_launch_ms, 4),
                  "algorithmic_bytes": b, "algorithmic_flops": f,
                  "peak_source": "own microbenchmark" if "own" in roof.get("peak_kind", "") else pk_src})
 

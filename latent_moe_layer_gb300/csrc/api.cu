@@ -336,6 +336,7 @@ int k3_ws_layout(const k3moe_handle *h, int T, void *base, k3_ws *ws)
     ws->meta = cv.take<int32_t>(16);
     ws->active = cv.take<int32_t>(c.n_experts);
     ws->tiles = cv.take<int32_t>(4 * (R + c.n_experts + 1));
+    ws->gv_sync = cv.take<int32_t>(2 + R + c.n_experts);
     ws->act = cv.take<float>(R * c.inter + 1);          // fp32 (generic) or f16 (tensor)
     ws->y = cv.take<float>(R * c.latent + 1);
     // Tensor-path expert inputs in expert order: f16 h [R, L] (decode GEMV and tcgen05

@@ -85,11 +85,12 @@ struct GvSmem {
 };
 
 // One work item's K loop for a tile of NNB x 8 token rows (the token count is a
-// template argument so that the unrolled loop carries no branches).  PRE: the next
+// template argument so that the unrolled loop carries no branches).  The stages have
+// the layout of LM >= NMAT matrices (the activation rows after them).  PRE: the next
 // work item's first-stage scale bytes (rows at sa_next, nullptr if none) are read
 // during the last stage and handed over in `carry`; with carry_in this item's come
 // from there.
-template <int NMAT, int NS, int WPC, int NNB, bool PRE>
+template <int NMAT, int LM, int NS, int WPC, int NNB, bool PRE>
 __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t *full, uint64_t *empty,
                                             volatile int *abort_flag, const GemvArgs &a, int nkp, int ra_l,
                                             int g8, int c, int lane, const uint2 *const (&sa)[NMAT],
@@ -98,7 +99,7 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
                                             float (&acc)[NMAT][2][4])
 {
     const int tr = tok_perm(g8);
-    using SM = GvSmem<NMAT, NS, WPC>;
+    using SM = GvSmem<LM, NS, WPC>;
     // scale bytes: 8 per row and stage (blocks 8s .. 8s+7), read one stage ahead
     uint2 sca[NMAT], scb[NMAT], nsa[NMAT], nsb[NMAT];
 #pragma unroll
@@ -127,7 +128,7 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
         const int slot = it % NS;
         if (!role_wait(smem_u32(full + slot), (it / NS) & 1, abort_flag, 0xFFFFFFFFu, a.status, 12)) return false;
         const uint8_t *sbase = smem + slot * SM::STAGE;
-        const uint8_t *bbase = sbase + NMAT * SM::MAT_BYTES;
+        const uint8_t *bbase = sbase + LM * SM::MAT_BYTES;
         // ldmatrix row base of this lane: tile (lane >> 3) = (matrix, rows ra or rb)
         const int cw_rows = ra_l >> 4;                   // this warp's 16-row group
         const uint32_t sld = smem_u32(sbase) + ((lane >> 4) & (NMAT - 1)) * SM::MAT_BYTES +
@@ -195,6 +196,44 @@ __device__ __forceinline__ bool gemv_k_loop(const uint8_t *smem, const uint64_t 
         }
     }
     return true;
+}
+
+// Output of one work item: acc[m][nb][0..1] = (row ra, tokens 8 nb + 2c, +1),
+// [2..3] = (row rb, same tokens).  PRE: pf holds each of the thread's two token
+// columns' input and output factors, read ahead.
+template <int NMAT, int MODE, int MAXNB, bool PRE>
+__device__ __forceinline__ void gemv_epilogue(const GemvArgs &a, const float (&acc)[NMAT][2][4],
+                                              const float (&pf)[2][2], int c, int ra, int rb, int b_first, int nt)
+{
+#pragma unroll
+    for (int nb = 0; nb < MAXNB; ++nb)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int tok = 8 * nb + tok_perm(2 * c + (q & 1));
+            const int row = (q < 2) ? ra : rb;
+            if (tok < nt) {
+                const size_t orow = (size_t)(b_first + tok);
+                if (MODE == GV_GLU_F16) {
+                    const float rs = PRE ? pf[q & 1][0] : (a.rscale ? __ldg(a.rscale + orow) : 1.f);
+                    const float gv = acc[0][nb][q] * rs;
+                    const float uv = acc[NMAT - 1][nb][q] * rs;
+                    const float av = k3_glu(gv, uv, a.act);
+                    if (a.out_f32) {
+                        reinterpret_cast<float *>(a.out)[orow * a.rows + row] = av;
+                    } else {
+                        // an exact power of two keeps |a| inside the f16 range
+                        const float asv = PRE ? pf[q & 1][1] : (a.ascale ? __ldg(a.ascale + orow) : 1.f);
+                        const float as = av * pow2_inverse(asv);
+                        if (!(fabsf(as) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
+                        reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(as);
+                    }
+                } else {
+                    const float asv = PRE ? pf[q & 1][1] : (a.ascale ? __ldg(a.ascale + orow) : 1.f);
+                    const float y = acc[0][nb][q] * asv;
+                    reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] = f32_to_bf16(y);
+                }
+            }
+        }
 }
 
 // MAXNB = 2: the K loop exists for 8- and 16-token tiles.  MAXNB = 1: for 8 only (tiles of
@@ -318,43 +357,238 @@ __global__ void __launch_bounds__((WPC + 1) * 32, 16 / WPC) gemv_expert_kernel(c
 #pragma unroll
                     for (int q = 0; q < 4; ++q) acc[m][h][q] = 0.f;
             const bool ok = (MAXNB == 2 && nt > 8)
-                                ? gemv_k_loop<NMAT, NS, WPC, 2, PRE>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
+                                ? gemv_k_loop<NMAT, NMAT, NS, WPC, 2, PRE>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
                                                                 sa, sa_next, have_carry, carry, kb, it, acc)
-                                : gemv_k_loop<NMAT, NS, WPC, 1, PRE>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
+                                : gemv_k_loop<NMAT, NMAT, NS, WPC, 1, PRE>(smem, full, empty, abort_flag, a, nkp, ra_l, g8, c, lane,
                                                                 sa, sa_next, have_carry, carry, kb, it, acc);
             if (!ok) break;
             have_carry = PRE && sa_next[0] != nullptr;
-            // epilogue: acc[m][nb][0..1] = (row ra, tokens 8 nb + 2c, +1); [2..3] = (row rb, same tokens)
-#pragma unroll
-            for (int nb = 0; nb < MAXNB; ++nb)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tok = 8 * nb + tok_perm(2 * c + (q & 1));
-                    const int row = (q < 2) ? ra : rb;
-                    if (tok < nt) {
-                        const size_t orow = (size_t)(b_first + tok);
-                        if (MODE == GV_GLU_F16) {
-                            const float rs = PRE ? pf[q & 1][0] : (a.rscale ? __ldg(a.rscale + orow) : 1.f);
-                            const float gv = acc[0][nb][q] * rs;
-                            const float uv = acc[NMAT - 1][nb][q] * rs;
-                            const float av = k3_glu(gv, uv, a.act);
-                            if (a.out_f32) {
-                                reinterpret_cast<float *>(a.out)[orow * a.rows + row] = av;
-                            } else {
-                                // an exact power of two keeps |a| inside the f16 range
-                                const float asv = PRE ? pf[q & 1][1] : (a.ascale ? __ldg(a.ascale + orow) : 1.f);
-                                const float as = av * pow2_inverse(asv);
-                                if (!(fabsf(as) <= 65504.f)) set_status(a.status, K3MOE_ERR_RANGE, 3);
-                                reinterpret_cast<__half *>(a.out)[orow * a.rows + row] = __float2half_rn(as);
-                            }
-                        } else {
-                            const float asv = PRE ? pf[q & 1][1] : (a.ascale ? __ldg(a.ascale + orow) : 1.f);
-                            const float y = acc[0][nb][q] * asv;
-                            reinterpret_cast<uint16_t *>(a.out)[orow * a.rows + row] = f32_to_bf16(y);
-                        }
-                    }
-                }
+            gemv_epilogue<NMAT, MODE, MAXNB, PRE>(a, acc, pf, c, ra, rb, b_first, nt);
         }
+    }
+}
+
+// ---- The decode gate/up and down GEMVs of one routing as one persistent launch
+// (8-token tiles, two CTAs of 8 consumer warps per SM).  Separate launches each end in
+// a partly idle round (the work items rarely divide evenly over the CTAs) and the down
+// launch starts only when the last gate/up CTA has finished.  Here each CTA's producer
+// takes work items in ticket order from a counter: first every (tile, 128-row block)
+// of gate/up, then every (tile, 256-row block) of down (two 128-row blocks of w2 in the
+// stage's two matrix slots, against the same activation rows, so that every stage has
+// the gate/up shape), and hands each to its consumer warps through a small ring in
+// shared memory.  A down item reads its tile's GLU output, so its producer first waits
+// until all gate/up items of that tile are stored: each consumer warp counts each
+// gate/up item it finished in the tile's counter, after a fence that it issues just
+// before its next item's epilogue (by then the stores are long done and the fence is
+// cheap), or at once when its next item is a down item or the end.  Tickets are taken
+// in order by running CTAs and a producer publishes an item before it waits on it, so
+// the gate/up items a down item waits for are held by running CTAs whose warps finish
+// and count them without waiting on anything.
+constexpr int GF_NI = 4;    // item ring slots
+
+template <int NS>
+struct GfSmem {
+    using SM = GvSmem<2, NS, 8>;
+    // the stage ring of the gate/up layout (down items use its first matrix slot), then
+    // full[NS], empty[NS], ifull[GF_NI], iempty[GF_NI], the abort flag and the item slots
+    static constexpr int OFF_BAR = SM::OFF_BAR;
+    static constexpr int OFF_FLAG = OFF_BAR + (2 * NS + 2 * GF_NI) * 8;
+    static constexpr int OFF_ITEMS = OFF_FLAG + 16;
+    static constexpr int BYTES = OFF_ITEMS + GF_NI * 4 + 1024;
+};
+
+// Waits (bounded) until the counter at p reaches target.
+__device__ __forceinline__ bool gf_wait_count(const int *p, int target, volatile int *abort_flag, int *status)
+{
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (i == 0) {
+            t0 = globaltimer();
+        } else if ((i & 255u) == 0 && globaltimer() - t0 > kWaitCapNs) {
+            set_status(status, K3MOE_ERR_TIMEOUT, 15);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+// a1: gate/up (GLU, f16 output, no read-ahead factors), a2: down (BF16 output); the same
+// tile list.  sync[0]: ticket counter; sync[1 + t]: finished gate/up item-warps of tile
+// t; both zero before the launch.
+template <int NS>
+__global__ void __launch_bounds__(288, 2) gemv_fused_kernel(const __grid_constant__ CUtensorMap bmap1,
+                                                            const __grid_constant__ CUtensorMap bmap2,
+                                                            const GemvArgs a1, const GemvArgs a2, int *sync)
+{
+    griddep_enter();
+    using SM = GvSmem<2, NS, 8>;
+    using GF = GfSmem<NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + GF::OFF_BAR), *empty = full + NS;
+    uint64_t *ifull = empty + NS, *iempty = ifull + GF_NI;
+    volatile int *abort_flag = (volatile int *)(smem + GF::OFF_FLAG);
+    volatile int *items = (volatile int *)(smem + GF::OFF_ITEMS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = __ldg(a1.n_tiles);
+    const int mt1 = a1.rows / 128, mt2 = a2.rows / 256;
+    const int total1 = n_tiles * mt1, total = total1 + n_tiles * mt2;
+    const int nkp1 = a1.K / 256, nkp2 = a2.K / 256;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 8);
+        }
+        for (int i = 0; i < GF_NI; ++i) {
+            mbar_init(smem_u32(ifull + i), 1);
+            mbar_init(smem_u32(iempty + i), 8);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ tickets and TMA
+        if (lane == 0) {
+            prefetch_tmap(&bmap1);
+            prefetch_tmap(&bmap2);
+            const uint64_t pol = policy_evict_first(), polb = policy_evict_last();
+            uint32_t it = 0, ii = 0;
+            // one ticket at a time: taking the next one an item ahead measured slower (0.7033 vs
+            // 0.6995 ms per T=16 step): a ticket held ahead cannot go to a CTA that is idle
+            while (!*abort_flag) {
+                const int islot = ii % GF_NI;
+                if (!role_wait(smem_u32(iempty + islot), ((ii / GF_NI) & 1) ^ 1, abort_flag, 0xFFFFFFFFu,
+                               a1.status, 13))
+                    break;
+                const int item = atomicAdd(sync, 1);
+                items[islot] = item < total ? item : -1;
+                mbar_arrive(smem_u32(ifull + islot));
+                ++ii;
+                if (item >= total) break;
+                const bool up = item < total1;
+                const int d = up ? item : item - total1, mt = up ? mt1 : mt2;
+                const int ti = d / mt, m0 = (d % mt) * (up ? 128 : 256);
+                const int4 tile = __ldg((up ? a1.tiles : a2.tiles) + ti);
+                const CUtensorMap *am = up ? a1.amaps + (size_t)tile.x * a1.amap_stride
+                                           : a2.amaps + (size_t)tile.x * a2.amap_stride;
+                const CUtensorMap *am0 = am + (up ? a1.amap_off[0] : a2.amap_off[0]);
+                const CUtensorMap *am1 = am + (up ? a1.amap_off[1] : a2.amap_off[0]);
+                const int m1 = up ? m0 : m0 + 128;                  // matrix slot 1: w3, or w2's next block
+                if (!up) {
+                    // the tile's GLU output, written by the gate/up items through the generic
+                    // proxy, is read here by TMA
+                    if (!gf_wait_count(sync + 1 + ti, 8 * mt1, abort_flag, a2.status)) break;
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                const CUtensorMap *bm = up ? &bmap1 : &bmap2;
+                const int nkp = up ? nkp1 : nkp2;
+                bool ok = true;
+                for (int s = 0; s < nkp; ++s, ++it) {
+                    const int slot = it % NS;
+                    if (!role_wait(smem_u32(empty + slot), ((it / NS) & 1) ^ 1, abort_flag, 0xFFFFFFFFu,
+                                   a1.status, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(full + slot);
+                    mbar_expect_tx(fb, SM::STAGE);
+                    uint8_t *dst = smem + slot * SM::STAGE;
+                    tma_load_2d_hint(smem_u32(dst), am0, fb, s * 128, m0, pol);
+                    tma_load_2d_hint(smem_u32(dst + SM::MAT_BYTES), am1, fb, s * 128, m1, pol);
+                    uint8_t *bdst = dst + 2 * SM::MAT_BYTES;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d_hint(smem_u32(bdst + q * 16 * 128), bm, fb, s * 256 + q * 64, tile.y, polb);
+                }
+                if (!ok) break;
+            }
+            drain_ring(full, it, NS);
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int cw = warp - 1;
+        const int g8 = lane >> 2, c = lane & 3;
+        const int ra_l = 16 * cw + g8;
+        const float pf[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+        int owed = -1;                          // tile whose counter this warp owes its last gate/up item
+        auto pay = [&]() {
+            if (owed >= 0) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(sync + 1 + owed, 1);
+                owed = -1;
+            }
+        };
+        uint32_t it = 0, ii = 0;
+        for (;;) {
+            const int islot = ii % GF_NI;
+            if (!role_wait(smem_u32(ifull + islot), (ii / GF_NI) & 1, abort_flag, 0xFFFFFFFFu, a1.status, 14))
+                break;
+            const int item = items[islot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(iempty + islot));
+            ++ii;
+            if (item < total1) {
+                if (item < 0) break;
+                const int ti = item / mt1, m0 = (item % mt1) * 128;
+                const int4 tile = __ldg(a1.tiles + ti);
+                const int ra = m0 + ra_l, rb = ra + 8;
+                const int kb = a1.K / 32;
+                const uint2 *sa[2], *sn[2] = {nullptr, nullptr};
+                uint2 carry[2][2];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+                    sa[m] = reinterpret_cast<const uint2 *>(a1.scales[m][tile.x] + (size_t)ra * kb);
+                float acc[2][2][4];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[m][h][q] = 0.f;
+                if (!gemv_k_loop<2, 2, NS, 8, 1, false>(smem, full, empty, abort_flag, a1, nkp1, ra_l, g8, c, lane,
+                                                        sa, sn, false, carry, kb, it, acc))
+                    break;
+                pay();
+                gemv_epilogue<2, GV_GLU_F16, 1, false>(a1, acc, pf, c, ra, rb, tile.y, tile.z);
+                owed = ti;
+            } else {
+                pay();
+                const int d = item - total1;
+                const int ti = d / mt2, m0 = (d % mt2) * 256;
+                const int4 tile = __ldg(a2.tiles + ti);
+                const int ra = m0 + ra_l, rb = ra + 8;
+                const int kb = a2.K / 32;
+                // matrix slot m: w2 rows m0 + 128 m ..
+                const uint2 *sa[2] = {reinterpret_cast<const uint2 *>(a2.scales[0][tile.x] + (size_t)ra * kb),
+                                      reinterpret_cast<const uint2 *>(a2.scales[0][tile.x] + (size_t)(ra + 128) * kb)};
+                const uint2 *sn[2] = {nullptr, nullptr};
+                uint2 carry[2][2];
+                float acc[2][2][4];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[m][h][q] = 0.f;
+                if (!gemv_k_loop<2, 2, NS, 8, 1, false>(smem, full, empty, abort_flag, a2, nkp2, ra_l, g8, c, lane,
+                                                        sa, sn, false, carry, kb, it, acc))
+                    break;
+                gemv_epilogue<1, GV_BF16, 1, false>(a2, reinterpret_cast<const float(&)[1][2][4]>(acc[0]), pf, c,
+                                                    ra, rb, tile.y, tile.z);
+                gemv_epilogue<1, GV_BF16, 1, false>(a2, reinterpret_cast<const float(&)[1][2][4]>(acc[1]), pf, c,
+                                                    ra + 128, rb + 128, tile.y, tile.z);
+            }
+        }
+        pay();
     }
 }
 
@@ -394,4 +628,19 @@ int k3_launch_gemv_expert(int glu, int mode, int max_nb, const CUtensorMap &bmap
         if (mode == GV_BF16) return launch_gemv<1, 4, GV_BF16, 2, 8>(bmap, args, max_items, num_sms, st);
     }
     return K3MOE_ERR_UNSUPPORTED;
+}
+
+int k3_launch_gemv_fused(const CUtensorMap &bmap1, const CUtensorMap &bmap2, const GemvArgs &a1, const GemvArgs &a2,
+                         int32_t *sync, int max_items, int num_sms, cudaStream_t st)
+{
+    using GF = GfSmem<2>;
+    static_assert(2 * GF::BYTES <= 228 * 1024, "two CTAs per SM");
+    if (a1.rows % 128 || a2.rows % 256 || a1.amap_off[0] == a1.amap_off[1]) return K3MOE_ERR_SHAPE;
+    auto kern = gemv_fused_kernel<2>;
+    static unsigned long long attr_set = 0;
+    if (!k3_smem_attr(kern, GF::BYTES, attr_set)) return K3MOE_ERR_CUDA;
+    const int grid = max(1, min(max_items, 2 * num_sms));
+    k3_launch(kern, grid, 288, GF::BYTES, st, bmap1, bmap2, a1, a2, sync);
+    k3_note_launch();
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

@@ -31,3 +31,9 @@ struct GemvArgs {
 // to 16 tokens; 1 for tiles of at most 8 (a kernel with fewer live registers).
 int k3_launch_gemv_expert(int glu, int mode, int max_nb, const CUtensorMap &bmap, const k3::GemvArgs &args,
                           int max_items, int num_sms, cudaStream_t st);
+// The gate/up (a1, GLU) and down (a2, BF16) GEMVs of one routing in one persistent launch,
+// 8-token tiles only: bmap1 over the f16 expert inputs [R, L], bmap2 over the GLU output
+// [R, I] (a1.out), both with 16-row boxes; a2.rows a multiple of 256 (down items are 256
+// rows).  sync: 1 + tiles ints, zero before the launch.  max_items bounds the grid.
+int k3_launch_gemv_fused(const CUtensorMap &bmap1, const CUtensorMap &bmap2, const k3::GemvArgs &a1,
+                         const k3::GemvArgs &a2, int32_t *sync, int max_items, int num_sms, cudaStream_t st);

@@ -255,6 +255,7 @@ struct k3_ws {
     int32_t *meta;        // small scalars: [0] = number of active experts, [1] = number of tiles
     int32_t *active;      // [E] active expert list
     int32_t *tiles;       // tensor-path tile list (int4 per tile)
+    int32_t *gv_sync;     // [2 + T*K + E] fused decode GEMV: ticket counter, then per-tile finished gate/up item-warps
     void *act;            // [T*K, I] fp32 (generic) or f16 (tensor path)
     void *y;              // [T*K, L] fp32 (generic) or BF16 (tensor path)
     void *hperm;          // [T*K, L] f16 (tensor path) activation rows in expert order

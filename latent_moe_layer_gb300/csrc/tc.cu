@@ -91,10 +91,14 @@ __global__ void __launch_bounds__(256) prep_f16_rows_kernel(const uint16_t *__re
                                                            __half *__restrict__ dst,
                                                            float *__restrict__ rscale,
                                                            const float *__restrict__ bound,
-                                                           float *__restrict__ ascale)
+                                                           float *__restrict__ ascale, int32_t *__restrict__ zero,
+                                                           int zero_n)
 {
     griddep_enter();
     const int t = blockIdx.x, tid = threadIdx.x;
+    // block (0, 0) also clears the fused decode GEMV's counters
+    if (zero && t == 0 && blockIdx.y == 0)
+        for (int i = tid; i < zero_n; i += blockDim.x) zero[i] = 0;
     const uint16_t *s = src + (size_t)t * cols;
     float amax = 0.f;
     for (int i = tid * 8; i < cols; i += 256 * 8) {
@@ -601,7 +605,8 @@ static int finish_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_
         {
             k3_stage sg(h, K3MOE_STAGE_PREP, st);
             k3_launch(prep_f16_rows_kernel, T, 256, 0, st, (const uint16_t *)x, H, nullptr, 1, (__half *)ws.xs,
-                      ws.xscale, c.act == K3MOE_ACT_SITU ? nullptr : (const float *)h->d_glu_bound + 2, ws.xascale);
+                      ws.xscale, c.act == K3MOE_ACT_SITU ? nullptr : (const float *)h->d_glu_bound + 2, ws.xascale,
+                      (int32_t *)nullptr, 0);
             k3_note_launch();
             k3_launch(dense_tiles_kernel, 1, 256, 0, st, T, sbn, stiles, ws.meta + 2);
             k3_note_launch();
@@ -658,6 +663,9 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
     // (an expert with more gets several tiles, each streaming its weights): its kernel for
     // 8-token tiles keeps more registers for the one K loop and runs faster.
     const int gv_nb = (size_t)T * K <= 2 * (size_t)E ? 1 : 2;
+    // Then (without A8, whose GLU output is rounded by a kernel of its own) the gate/up and
+    // down GEMVs run as one persistent launch, so that neither ends in a partly idle round.
+    const bool gv_fused = gemv && gv_nb == 1 && !c.a8 && L % 256 == 0;
     const bool mx = c.a8 && !gemv;              // A8 at tile sizes: block-scaled MXFP4 x MXFP8 MMAs
     const int bn = mx ? MX_BN : pick_bn(T, K, E);
     int rc;
@@ -717,7 +725,7 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         // through the GEMV keeps the GLU output in fp32 until its MXFP8 rounding, which applies it
         k3_launch(prep_f16_rows_kernel, dim3(T, prep_split(T, K, h->num_sms)), 256, 0, st, ws.h, L, ws.row_of, K,
                   (__half *)ws.hperm, ws.hscale, c.act == K3MOE_ACT_SITU ? nullptr : (const float *)h->d_glu_bound,
-                  ws.ascale);
+                  ws.ascale, gv_fused ? ws.gv_sync : (int32_t *)nullptr, 2 + R + E);
         k3_note_launch();
         K3_CUDA_TRY(cudaGetLastError());
     }
@@ -785,6 +793,15 @@ int k3_forward_tc(k3moe_handle *h, const void *x, int T, void *out, const k3_ws 
         g2.rscale = nullptr;
         g2.ascale = ws.ascale;
         g2.out = ws.y;
+        if (gv_fused) {
+            // both projections in one launch (stage timing: all of it under gate/up)
+            k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
+            CUtensorMap gb1, gb2;
+            if (!encode_act(&gb1, ws.hperm, R, L, 16) || !encode_act(&gb2, act16, R, I, 16)) return K3MOE_ERR_CUDA;
+            const int items = max_ntiles * std::max(I / 128, L / 128);
+            if ((rc = k3_launch_gemv_fused(gb1, gb2, g1, g2, ws.gv_sync, items, h->num_sms, st))) return rc;
+            return finish_tc(h, x, T, out, ws, st);
+        }
         {
             k3_stage sg(h, K3MOE_STAGE_GATE_UP, st);
             CUtensorMap gb1;
