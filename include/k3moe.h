@@ -186,7 +186,10 @@ int k3moe_forward_host(k3moe_handle *h, const void *x_host, int T, void *out_hos
                        cudaStream_t stream);
 
 /* Synchronise `stream`, read and clear the device status word: K3MOE_OK or
- * the first device-side error recorded since the last call. */
+ * the first device-side error recorded since the last call.  After an error it
+ * also clears the decode-size dense GEMMs' split-K arrival counters (kept in the
+ * persistent buffer): a kernel stopped by a timeout may have left them part-way.
+ * Forwards enqueued after a failure and before this call may be wrong. */
 int k3moe_status(k3moe_handle *h, cudaStream_t stream);
 
 /* Destroy the handle (host only; frees no caller memory).  NULL is allowed. */
