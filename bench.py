@@ -106,6 +106,18 @@ def stage_work(cfg, touched, path_tensor):
     return w
 
 
+def dominant_stage(stage_ms, work):
+    """The stage with the largest time, its (bytes, flops) and whether it is the fused
+    decode GEMV launch: that one is timed as the gate/up stage (no expert_down time) and
+    does both projections' work."""
+    fused = stage_ms.get("gate_up", 0) > 0 and stage_ms.get("expert_down", 0) == 0
+    if fused:
+        work = dict(work)
+        work["gate_up"] = tuple(u + v for u, v in zip(work["gate_up"], work["expert_down"]))
+    dom = max(stage_ms, key=lambda s: stage_ms[s])
+    return dom, work[dom], fused
+
+
 def load_summary(load, cfg, path_tensor):
     """Rows per expert (histogram over experts) and the tile padding of the expert GEMMs."""
     import numpy as np
@@ -359,14 +371,8 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
     value = whole_job_value(cfg.T, args.steps, total_ms, world)
 
     # roofline of the dominant stage
-    work = stage_work(cfg, touched, path_tensor)
-    # the decode GEMVs of both projections can run as one launch, timed as the gate/up stage
-    fused = stage_ms.get("gate_up", 0) > 0 and stage_ms.get("expert_down", 0) == 0
-    if fused:
-        work["gate_up"] = tuple(u + v for u, v in zip(work["gate_up"], work["expert_down"]))
-    dom = max(stage_ms, key=lambda s: stage_ms[s])
+    dom, (b, f), fused = dominant_stage(stage_ms, stage_work(cfg, touched, path_tensor))
     per_launch_ms = stage_ms[dom] / max(1, nfw)
-    b, f = work[dom]
     decode = cfg.T <= 256
     if decode or f == 0:
         ach = b / (per_launch_ms / 1e3) / 1e9
