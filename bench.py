@@ -371,7 +371,8 @@ def measure(cfg, dw, args, ctx, cpu_seconds, extras=True):
     value = whole_job_value(cfg.T, args.steps, total_ms, world)
 
     # roofline of the dominant stage
-    dom, (b, f), fused = dominant_stage(stage_ms, stage_work(cfg, touched, path_tensor))
+    work = stage_work(cfg, touched, path_tensor)
+    dom, (b, f), fused = dominant_stage(stage_ms, work)
     per_launch_ms = stage_ms[dom] / max(1, nfw)
     decode = cfg.T <= 256
     if decode or f == 0:
