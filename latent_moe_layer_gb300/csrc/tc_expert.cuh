@@ -81,7 +81,10 @@ struct ExpertSmem {
     static constexpr int OFF_BAR = OFF_PK + NS * NMAT * PK_BYTES;
     static constexpr int N_BAR = 2 * NS + 2 * NB + 2 * NA + 4 + 1 + 2;
     static constexpr int OFF_RS = (OFF_BAR + N_BAR * 8 + 16 + 15) & ~15;   // after the tmem holder and abort flag; 16-byte reads
-    static constexpr int BYTES = OFF_RS + BN * 4 + BN + 1024;         // + per-token factors and exponents + align slack
+    // per-token factors (fp32), then the GLU output divisors' exponents: as fp32 factors
+    // already multiplied into the input factor (RSA) where shared memory allows, else as bytes
+    static constexpr bool RSA = OFF_RS + BN * 8 + 1024 <= 227 * 1024;
+    static constexpr int BYTES = OFF_RS + BN * 4 + (RSA ? BN * 4 : BN) + 1024;   // + align slack
 };
 
 __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
@@ -93,13 +96,28 @@ __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
 }
 
 // Wait with the CTA abort flag: returns false on timeout or abort.
+// try_wait with a suspend-time hint of 20 us: a waiting thread sleeps until the phase
+// completes (or the hint runs out) instead of spinning on the issue slots its warp shares
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           uint32_t limit, int *status, int where)
 {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     for (uint32_t i = 1; i < limit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity)) return true;
         if (*abort_flag) return false;
         if ((i & 255u) == 0 && globaltimer() - t0 > kWaitCapNs) break;
     }
@@ -153,6 +171,9 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = args.K, nkp = K / EX_KP;
+    // SiLU: the GLU output divisor 2^-k is staged multiplied into the up branch's input factor
+    // (SiTU soft-limits the up branch, so its factor stays apart)
+    constexpr bool RSA = SM::RSA && MODE == OUT_GLU_F16 && EPI == EPI_SILU;
     // GLU: the two matrices share the job's 128 rows.  Otherwise NMAT = 2 takes two
     // 128-row blocks of the same matrix, so each activation tile feeds 256 rows.
     constexpr bool ROWPAIR = MODE != OUT_GLU_F16 && NMAT == 2;
@@ -455,8 +476,13 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 uint8_t *sas = reinterpret_cast<uint8_t *>(srs + BN);
                 for (int i = eth; i < nrows; i += NEPI * 32) {
                     srs[i] = args.rscale ? __ldg(args.rscale + row0 + i) : 1.f;
-                    if (MODE == OUT_GLU_F16)     // k of the output's divisor 2^k, one byte
-                        sas[i] = args.ascale ? (uint8_t)((__float_as_uint(__ldg(args.ascale + row0 + i)) >> 23) - 127) : 0;
+                    if (MODE == OUT_GLU_F16) {   // k of the output's divisor 2^k
+                        const uint32_t k = args.ascale ? (__float_as_uint(__ldg(args.ascale + row0 + i)) >> 23) - 127 : 0;
+                        if constexpr (RSA)
+                            reinterpret_cast<float *>(sas)[i] = srs[i] * __uint_as_float((127u - k) << 23);
+                        else
+                            sas[i] = (uint8_t)k;
+                    }
                 }
                 mbar_arrive(smem_u32(rsfull));
                 if (!role_wait(smem_u32(rsfull), tc & 1, abort_flag, lim, args.status, 9)) break;
@@ -495,7 +521,17 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         rsv[4 * w + 3] = f.w;
                     }
                 }
-                if constexpr (MODE == OUT_GLU_F16 && KIND != EPI_A8) {
+                if constexpr (MODE == OUT_GLU_F16 && RSA) {
+                    // the input factor times 2^-k, for the up branch
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 f = reinterpret_cast<const float4 *>(srs + BN + c * 16)[w];
+                        asv[4 * w] = f.x;
+                        asv[4 * w + 1] = f.y;
+                        asv[4 * w + 2] = f.z;
+                        asv[4 * w + 3] = f.w;
+                    }
+                } else if constexpr (MODE == OUT_GLU_F16 && KIND != EPI_A8) {
                     const uint4 e = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(srs + BN) + c * 16);
                     const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
@@ -542,37 +578,45 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         }
                     }
                 } else {
+                    // the chunk's 16 results first, without branches, so that their dependency
+                    // chains interleave (columns past the tile's rows give values that are never
+                    // stored), then the stores of the columns the tile holds
+                    uint32_t o0[16], o1[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int n = c * 16 + j;
-                        if (n < nrows) {
-                            const size_t orow = (size_t)(row0 + n);
-                            if (MODE == OUT_GLU_F16) {
-                                // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
-                                // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
-                                // beta tanh(gv / beta) and soft-limits the up branch the same way
-                                const float rs = rsv[j];
-                                const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
-                                const float uv = __uint_as_float(v1[j]) * (fw1 * rs);
-                                float a;
-                                if constexpr (KIND == EPI_SITU)
-                                    a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
-                                        tanh_approx(hv * (2.0f * args.act.inv_beta)) *
-                                        (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
-                                else
-                                    a = fmaf(hv, tanh_approx(hv), hv) * uv;
-                                a *= asv[j];                // exact power of two keeping |a| inside f16
-                                bad |= !(fabsf(a) <= 65504.f);
-                                reinterpret_cast<__half *>(args.out)[orow * args.rows + row] = __float2half_rn(a);
-                            } else if (MODE == OUT_BF16) {
-                                uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                                o[row] = f32_to_bf16(__uint_as_float(v0[j]) * (fw0 * rsv[j]));
-                                if (ROWPAIR) o[row1] = f32_to_bf16(__uint_as_float(v1[j]) * (fw1 * rsv[j]));
-                            } else {
-                                uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + orow * args.rows;
-                                o[row] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * (fw0 * rsv[j]));
-                                if (ROWPAIR) o[row1] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * (fw1 * rsv[j]));
-                            }
+                        if (MODE == OUT_GLU_F16) {
+                            // sigmoid(gv) = (1 + tanh(hv)) / 2 with hv = gv / 2, so
+                            // SiLU(gv) = hv + hv tanh(hv); SiTU multiplies the sigmoid by
+                            // beta tanh(gv / beta) and soft-limits the up branch the same way
+                            const float rs = rsv[j];
+                            const float hv = __uint_as_float(v0[j]) * (0.5f * fw0 * rs);
+                            // RSA (SiLU): 2^-k is already in the up factor (an exact power of two)
+                            const float uv = __uint_as_float(v1[j]) * (fw1 * (RSA ? asv[j] : rs));
+                            float a;
+                            if constexpr (KIND == EPI_SITU)
+                                a = fmaf(0.5f, tanh_approx(hv), 0.5f) * args.act.beta *
+                                    tanh_approx(hv * (2.0f * args.act.inv_beta)) *
+                                    (args.act.linear_beta * tanh_approx(uv * args.act.inv_linear_beta));
+                            else
+                                a = fmaf(hv, tanh_approx(hv), hv) * uv;
+                            if (!RSA) a *= asv[j];      // exact power of two keeping |a| inside f16
+                            bad |= (c * 16 + j < nrows) && !(fabsf(a) <= 65504.f);
+                            o0[j] = __half_as_ushort(__float2half_rn(a));
+                        } else if (MODE == OUT_BF16) {
+                            o0[j] = f32_to_bf16(__uint_as_float(v0[j]) * (fw0 * rsv[j]));
+                            if (ROWPAIR) o1[j] = f32_to_bf16(__uint_as_float(v1[j]) * (fw1 * rsv[j]));
+                        } else {
+                            o0[j] = f32_to_bf16(ad0[j] + __uint_as_float(v0[j]) * (fw0 * rsv[j]));
+                            if (ROWPAIR) o1[j] = f32_to_bf16(ad1[j] + __uint_as_float(v1[j]) * (fw1 * rsv[j]));
+                        }
+                    }
+                    uint16_t *o = reinterpret_cast<uint16_t *>(args.out) + (size_t)(row0 + c * 16) * args.rows;
+                    const int nv = nrows - c * 16;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (j < nv) {
+                            o[(size_t)j * args.rows + row] = (uint16_t)o0[j];
+                            if (MODE != OUT_GLU_F16 && ROWPAIR) o[(size_t)j * args.rows + row1] = (uint16_t)o1[j];
                         }
                     }
                 }
