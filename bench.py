@@ -38,19 +38,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu captures of 128-expert cases at the K3 shapes, scaled by the touched experts:
 # the fused gate/up + down launch at T=16 (8-token tiles), the separate 16-token-tile
 # launches at T=37 (4.6 rows per expert, as at T=256 with 896 experts).  They hold for
-# the kernel source whose sha256 prefix is given; any other source reports traffic
-# null until it is captured again.
-NCU_TRAFFIC = {"source": "latent_moe_layer_gb300/csrc/gemv_expert.cu", "sha256_16": "3d9e64c1e7225346",
+# the kernel sources (the .cu and the headers it includes) whose concatenation has the
+# sha256 prefix given; any other source reports traffic null until it is captured again.
+_CS = "latent_moe_layer_gb300/csrc/"
+NCU_TRAFFIC = {"sources": [_CS + f for f in ("gemv_expert.cu", "gemv_expert.h", "wait.cuh", "ptx.cuh",
+                                             "k3moe_internal.h")],
+               "sha256_16": "6fe8398cb6a18084",
                "per_expert": {("gate_up+expert_down", "gemv"): 18.37e6, ("gate_up", "gemv"): 12.24e6,
                               ("expert_down", "gemv"): 5.883e6}}
 EXTRA_WORKLOADS = [2, 3, 4, "moderate", "3a8"]
 
 
+def sources_sha16(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic_per_expert():
-    p = os.path.join(ROOT, NCU_TRAFFIC["source"])
     try:
-        with open(p, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        sha = sources_sha16(NCU_TRAFFIC["sources"])
     except OSError:
         return {}
     return NCU_TRAFFIC["per_expert"] if sha == NCU_TRAFFIC["sha256_16"] else {}

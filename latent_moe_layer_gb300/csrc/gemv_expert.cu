@@ -19,7 +19,7 @@
 // and added to the row's accumulator (packed fp32x2 FMAs: the two token columns a
 // thread holds for one row share the row's scale).
 #include "gemv_expert.h"
-#include "tc_expert.cuh"
+#include "wait.cuh"
 
 namespace k3 {
 

@@ -29,6 +29,7 @@
 
 #include "k3moe_internal.h"
 #include "ptx.cuh"
+#include "wait.cuh"
 
 namespace k3 {
 
@@ -93,47 +94,6 @@ __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
     if (d >= -14) return (uint32_t)(d + 15) << 10;
     if (d >= -24) return 1u << (d + 24);
     return 0u;
-}
-
-// Wait with the CTA abort flag: returns false on timeout or abort.
-// try_wait with a suspend-time hint of 20 us: a waiting thread sleeps until the phase
-// completes (or the hint runs out) instead of spinning on the issue slots its warp shares
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(20000u)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          uint32_t limit, int *status, int where)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer();
-    for (uint32_t i = 1; i < limit; ++i) {
-        if (mbar_try_wait_hint(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitCapNs) break;
-    }
-    set_status(status, K3MOE_ERR_TIMEOUT, where);
-    *abort_flag = 1;
-    return false;
-}
-
-// Drain: wait (wall-clock bounded) for the last min(n, ring) uses of a TMA ring.
-__device__ __forceinline__ void drain_ring(uint64_t *full, uint32_t issued, int ring)
-{
-    const uint32_t n = issued < (uint32_t)ring ? issued : (uint32_t)ring;
-    for (uint32_t q = 0; q < n; ++q) {
-        const uint32_t i2 = issued - 1 - q;
-        mbar_wait(smem_u32(full + i2 % ring), (i2 / ring) & 1, 0xFFFFFFFFu);
-    }
 }
 
 // Threads per CTA: 4 control warps, 4 dequant warps per weight matrix (one thread

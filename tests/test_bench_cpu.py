@@ -36,13 +36,17 @@ def test_fused_decode_launch_counts_both_projections():
 
 
 def test_traffic_figure_needs_the_measured_source(tmp_path, monkeypatch):
-    src = tmp_path / "kernel.cu"
-    src.write_bytes(b"__global__ void k() {}\n")
-    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    rec = {"source": str(src), "sha256_16": sha, "per_expert": {("gate_up", "gemv"): 1.0}}
+    src, hdr = tmp_path / "kernel.cu", tmp_path / "kernel.cuh"
+    src.write_bytes(b"#include \"kernel.cuh\"\n__global__ void k() {}\n")
+    hdr.write_bytes(b"#define W 1\n")
+    sha = hashlib.sha256(src.read_bytes() + hdr.read_bytes()).hexdigest()[:16]
+    rec = {"sources": [str(src), str(hdr)], "sha256_16": sha, "per_expert": {("gate_up", "gemv"): 1.0}}
     monkeypatch.setattr(bench, "NCU_TRAFFIC", rec)
     monkeypatch.setattr(bench, "ROOT", "/")
     assert bench.ncu_traffic_per_expert() == {("gate_up", "gemv"): 1.0}
-    src.write_bytes(b"__global__ void k() { }\n")        # any edit of the kernel source
+    hdr.write_bytes(b"#define W 2\n")                  # an edit of a header the kernel includes
     assert bench.ncu_traffic_per_expert() == {}
-
+    hdr.write_bytes(b"#define W 1\n")
+    assert bench.ncu_traffic_per_expert() == {("gate_up", "gemv"): 1.0}
+    src.write_bytes(b"#include \"kernel.cuh\"\n__global__ void k() { }\n")   # or of the kernel itself
+    assert bench.ncu_traffic_per_expert() == {}
