@@ -241,7 +241,7 @@ int launch_expert(const ActMaps &bmap, const ExpertGemmArgs &a, int max_tiles, i
     static unsigned long long attr_set = 0;
     if (!k3_smem_attr(kern, SM::BYTES, attr_set)) return K3MOE_ERR_CUDA;
     const int grid = max(1, min(num_sms, max_tiles));
-    k3_launch(kern, grid, ex_threads(NMAT), SM::BYTES, st, bmap, a);
+    k3_launch(kern, grid, ex_threads(NMAT, ex_nepi(BN, MODE, EPI)), SM::BYTES, st, bmap, a);
     k3_note_launch();
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }

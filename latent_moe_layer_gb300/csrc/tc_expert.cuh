@@ -97,18 +97,25 @@ __device__ __forceinline__ uint32_t f16_pow2_bits(int d)
 }
 
 // Threads per CTA: 4 control warps, 4 dequant warps per weight matrix (one thread
-// per weight row) and 8 epilogue warps (two per TMEM lane quarter, alternating
-// 16-token chunks).
-constexpr int EX_NEPI = 8;
-__host__ __device__ constexpr int ex_threads(int nmat) { return (4 + 4 * nmat + EX_NEPI) * 32; }
+// per weight row) and the epilogue warps, ex_nepi of them (two or three per TMEM lane
+// quarter, taking 16-token chunks in turn).  The kernels with one accumulator set, whose
+// drain holds back the next job's MMAs, take three per quarter where their registers
+// fit the 80 a thread gets at 768 threads: the 192-token kernels (with their dequant
+// warps reading each sub-step's bytes when needed) and the SiLU GLU kernel of 256-token
+// tiles.  The others keep two.
+__host__ __device__ constexpr int ex_nepi(int bn, int mode, int epi)
+{
+    return bn == 192 || (bn == 256 && mode == 0 && epi == 0) ? 12 : 8;
+}
+__host__ __device__ constexpr int ex_threads(int nmat, int nepi) { return (4 + 4 * nmat + nepi) * 32; }
 
 template <int NMAT, int BN, int NS, int NB, int NA, int NACC, int MODE, bool ATMEM = false, int EPI = 0>
-__global__ void __launch_bounds__(ex_threads(NMAT), 1)
+__global__ void __launch_bounds__(ex_threads(NMAT, ex_nepi(BN, MODE, EPI)), 1)
 expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs args)
 {
     griddep_enter();
     using SM = ExpertSmem<NMAT, BN, NS, NB, NA, ATMEM>;
-    constexpr int DQW = 4, NEPI = EX_NEPI;
+    constexpr int DQW = 4, NEPI = ex_nepi(BN, MODE, EPI);
     constexpr int EPI_WARP0 = 4 + DQW * NMAT;
     // TMEM columns: NACC accumulator sets (2: the epilogue overlaps the next tile),
     // then with ATMEM the NA x NMAT decoded A sub-tiles (128 lanes x 32 columns each)
@@ -333,13 +340,18 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                 }
                 // the row's 128 packed bytes (128-byte swizzle of the TMA box)
                 const uint8_t *pk = smem + SM::OFF_PK + (slot * NMAT + mat) * SM::PK_BYTES + r * 128;
-                uint4 c[8];
+                // A in shared memory: the row's 128 bytes are read at once and the stage is
+                // released; ATMEM: each sub-step reads its own 32 bytes (fewer live registers,
+                // which leaves room for more epilogue warps) and the last one releases it
+                uint4 c[ATMEM ? 1 : 8];
+                if constexpr (!ATMEM) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (j ^ (r & 7)));
-                // the stage is refilled by TMA (async proxy): order these generic reads before it
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(pempty + slot));
+                    for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4 *>(pk + 16 * (j ^ (r & 7)));
+                    // the stage is refilled by TMA (async proxy): order these generic reads before it
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(pempty + slot));
+                }
                 const uint32_t sw_lo = (s & 1) ? sc_cur.z : sc_cur.x;
                 const uint32_t sw_hi = (s & 1) ? sc_cur.w : sc_cur.y;
 #pragma unroll
@@ -358,7 +370,19 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
                         break;
                     }
                     uint8_t *arow = smem + SM::OFF_A + (aslot * NMAT + mat) * SM::A_BYTES + r * 128;
-                    const uint4 lo = c[2 * q], hi = c[2 * q + 1];
+                    uint4 lo, hi;
+                    if constexpr (ATMEM) {
+                        lo = *reinterpret_cast<const uint4 *>(pk + 16 * ((2 * q) ^ (r & 7)));
+                        hi = *reinterpret_cast<const uint4 *>(pk + 16 * ((2 * q + 1) ^ (r & 7)));
+                        if (q == EX_NSUB - 1) {
+                            fence_proxy_async_smem();       // before the stage's refill by TMA
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(pempty + slot));
+                        }
+                    } else {
+                        lo = c[2 * q];
+                        hi = c[2 * q + 1];
+                    }
                     const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     uint32_t tv[ATMEM ? 32 : 1];                 // ATMEM: the row's 64 values in K order
                     if (ATMEM) tc_fence_after();
@@ -413,7 +437,7 @@ expert_gemm_kernel(const __grid_constant__ ActMaps bmaps, const ExpertGemmArgs a
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                            // TMEM lanes 32q .. 32q+31
-        const int half = (warp - EPI_WARP0) >> 2;          // chunks c with c % 2 == half
+        const int half = (warp - EPI_WARP0) >> 2;          // chunks c with c % (NEPI / 4) == half
         const int eth = (warp - EPI_WARP0) * 32 + lane;
         const int r = q * 32 + lane;
         float *srs = reinterpret_cast<float *>(smem + SM::OFF_RS);
