@@ -19,9 +19,9 @@
 //   warp 2            TMA producer of the f16 activation sub-tiles (64 K x N rows)
 //   warp 1            TMEM allocator and the single MMA-issuing thread
 //   warps 4..4+4*NMAT dequant: one thread per weight row, FP4 -> f16 into the
-//                     128-byte-swizzled K-major layout the MMA reads
-//   last 8 warps      epilogue: TMEM -> registers -> scaled outputs, two warps per
-//                     TMEM lane quarter taking alternate 16-token chunks
+//                     128-byte-swizzled K-major layout the MMA reads, or into TMEM
+//   last 8 or 12      epilogue: TMEM -> registers -> scaled outputs, two or three
+//   warps             warps per TMEM lane quarter taking 16-token chunks in turn
 // Every wait is bounded; on expiry the CTA records K3MOE_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
 #pragma once
