@@ -67,8 +67,12 @@ __device__ __forceinline__ DnTile dn_tile(const DenseArgs &args, int t, int mt_n
     const DenseSeg S = dn_seg(args, r.seg);
     r.split = t % S.splits;
     t /= S.splits;
-    r.m0 = (t % mt_n) * DN_BM;
-    r.n0 = (t / mt_n) * BN;
+    // groups of G token tiles, token tile fastest within a group
+    const int G = S.m_group > 0 && S.m_group < mt_n ? S.m_group : mt_n;
+    const int per = G * S.n_tiles, g = t / per, w = t % per;
+    const int gs = min(G, mt_n - g * G);
+    r.m0 = (g * G + w % gs) * DN_BM;
+    r.n0 = (w / gs) * BN;
     // split s of KS K steps covers [s KS / splits, (s + 1) KS / splits): sizes differ by at most one
     const int KS = S.K / DN_BK;
     r.k0 = r.split * KS / S.splits;

@@ -16,6 +16,8 @@ struct DenseSeg {
     int K;           // reduction length (multiple of 64)
     int a_kmod;      // X column = k % a_kmod (router hi/lo: H; otherwise K)
     int mode;        // DN_OUT_F32: out[(split * M + m) * ldo + col0 + n]; DN_OUT_BF16: out[m * ldo + col0 + n]
+    int m_group;     // token-major kernel: the tiles of m_group token tiles (all n tiles) run before the next
+                     // group's, so the group's activation rows and the weights stay in L2; 0 = all token tiles
     void *out;
     int ldo;
     int col0;

@@ -419,6 +419,14 @@ static bool dense_small(const k3_ws &ws, int T, size_t width)
     return T <= 256 && ws.part_floats >= (size_t)K3_DENSE_MAX_SPLITS * T * width;
 }
 
+// Token tiles per group of the token-major dense GEMM: about 32 MiB of activation rows
+// (K columns of BF16), which with the weights (at most 51 MB here) stays inside the
+// 129 MB L2 while every weight tile passes over the group.  Without groups each wave of
+// tiles re-reads all the activation rows from HBM once T x K no longer fits in L2
+// (T=32768: router + down_proj 2.15 -> 1.94 ms, up_proj 1.57 -> 1.38 ms; 64 and 16 MiB
+// groups measured within 2% of 32).
+static int dense_m_group(int K) { return max(1, (32 << 20) / (128 * K * 2)); }
+
 // Router logits (fp32) and the latent h (BF16) in one tcgen05 launch.
 static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws &ws, cudaStream_t st)
 {
@@ -469,6 +477,7 @@ static int dense_router_down(k3moe_handle *h, const void *x, int T, const k3_ws 
         }
     } else {
         r.splits = d.splits = 1;
+        r.m_group = d.m_group = dense_m_group(H);
         r.mode = DN_OUT_F32;
         r.out = ws.logits;
         r.ldo = E;
@@ -519,6 +528,7 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
     u.col0 = 0;
     u.ldo = H;
     u.splits = 1;
+    u.m_group = dense_m_group(L);
     if (small) dense_splits(h, a.seg, 1, T, 2, dense_ws(T));
     u.out = small ? (void *)ws.part : (out16 ? (void *)out16 : (void *)ws.o32);
     if (ws_k) {
