@@ -547,18 +547,19 @@ static int dense_up(k3moe_handle *h, int T, const k3_ws &ws, uint16_t *out16, cu
 
 // Ring depths per tile shape: (packed stages NS, activation slots NB, f16 A slots NA,
 // accumulator sets NACC).  N <= 32 (shared experts at small T): gate/up 3/4/2/2
-// (176 KB smem), down 4/4/4/2 (144 KB).  N <= 192: both 3/5/2/1 with the A slots
-// in TMEM (2 x 192 accumulator + 2 x 2 x 32 A columns = 512; 216 KB smem).
+// (176 KB smem), down 4/4/4/2 (144 KB).  N <= 192: both 4/4/2/1 with the A slots
+// in TMEM (2 x 192 accumulator + 2 x 2 x 32 A columns = 512; 227 KB smem): their
+// dequant warps hold a packed stage until its last sub-step, so a fourth stage
+// beats a fifth activation slot (T=8192: gate/up 4.88 vs 4.91 ms with 3/5).
 // N <= 256: both 2/3/2/1 (224 KB; 512 TMEM columns).  The down projection takes
 // 256 weight rows per job (two 128-row blocks against one activation tile,
-// halving activation traffic).  Activation loads are latency-bound, so spare
-// shared memory goes to activation slots.
+// halving activation traffic).
 // The gate/up GEMM of tile shape bn with GLU variant EPI.
 template <int EPI>
 static int launch_glu(int bn, const ActMaps &b1, const ExpertGemmArgs &a1, int max_tiles1, int ns, cudaStream_t st)
 {
     return bn == 32    ? launch_expert<2, 32, 3, 4, 2, 2, OUT_GLU_F16, false, EPI>(b1, a1, max_tiles1, ns, st)
-           : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_GLU_F16, true, EPI>(b1, a1, max_tiles1, ns, st)
+           : bn == 192 ? launch_expert<2, 192, 4, 4, 2, 1, OUT_GLU_F16, true, EPI>(b1, a1, max_tiles1, ns, st)
                        : launch_expert<2, 256, 2, 3, 2, 1, OUT_GLU_F16, false, EPI>(b1, a1, max_tiles1, ns, st);
 }
 
@@ -585,7 +586,7 @@ static int expert_pair(k3moe_handle *h, int bn, const ActMaps &b1, const ActMaps
                           : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16_ADD>(b2, a2, max_tiles2, ns, st);
         else
             rc = bn == 32    ? launch_expert<1, 32, 4, 4, 4, 2, OUT_BF16>(b2, a2, max_tiles2, ns, st)
-                 : bn == 192 ? launch_expert<2, 192, 3, 5, 2, 1, OUT_BF16, true>(b2, a2, max_tiles2, ns, st)
+                 : bn == 192 ? launch_expert<2, 192, 4, 4, 2, 1, OUT_BF16, true>(b2, a2, max_tiles2, ns, st)
                              : launch_expert<2, 256, 2, 3, 2, 1, OUT_BF16>(b2, a2, max_tiles2, ns, st);
     }
     return rc;
